@@ -1,0 +1,157 @@
+"""Seeded synthetic inputs for the attention block.
+
+This module holds no arithmetic of the method: it only draws sequence lengths
+and fused-Wqkv rows from seeded torch CPU generators, so that the oracle and
+the CUDA path are fed identical inputs.  The shapes follow the ModernBERT-base
+model the pages describe (12 heads x 64, up to 8192 tokens per sequence,
+22 layers, layer i global iff i % 3 == 0); no page names a dataset for this
+path.
+
+Recipe: ``g = torch.Generator('cpu').manual_seed(seed)``; sequence lengths are
+drawn first with ``torch.randint(lo, hi + 1, (1,), generator=g)``; then
+``qkv = torch.randn(T, 2304, generator=g) * sigma`` rounded to bf16.
+"""
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+WIDTH = 2304          # 3 * 12 heads * 64
+OUT_WIDTH = 768
+N_LAYERS = 22
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    sigma: float
+    lengths: List[int]
+    kinds: List[str]
+    qkv: torch.Tensor = field(repr=False)          # bf16 [T, 2304], CPU
+    cu_seqlens: torch.Tensor = field(repr=False)   # int32 [n+1], CPU
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def n_seqs(self) -> int:
+        return len(self.lengths)
+
+    @property
+    def max_seqlen(self) -> int:
+        return max(self.lengths) if self.lengths else 0
+
+
+def cu_from_lengths(lengths) -> torch.Tensor:
+    cu = [0]
+    for L in lengths:
+        cu.append(cu[-1] + int(L))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def draw_qkv(g: torch.Generator, T: int, sigma: float) -> torch.Tensor:
+    x = torch.randn(T, WIDTH, generator=g, dtype=torch.float32)
+    if sigma != 1.0:
+        x.mul_(sigma)
+    return x.to(torch.bfloat16)
+
+
+def custom(lengths, seed: int, sigma: float = 1.0, kinds=("global", "local"),
+           name: Optional[str] = None) -> Workload:
+    g = torch.Generator().manual_seed(seed)
+    lengths = [int(L) for L in lengths]
+    cu = cu_from_lengths(lengths)
+    qkv = draw_qkv(g, int(cu[-1]), sigma)
+    return Workload(name or f"custom{lengths}", seed, sigma, lengths, list(kinds), qkv, cu)
+
+
+def _uniform_lengths(g, n, lo, hi):
+    return [int(torch.randint(lo, hi + 1, (1,), generator=g)) for _ in range(n)]
+
+
+def _fill_lengths(g, total, lo, hi):
+    """Draw L ~ U{lo..hi} until the next draw would overflow `total`; the last
+    sequence takes the remainder."""
+    out, acc = [], 0
+    while True:
+        L = int(torch.randint(lo, hi + 1, (1,), generator=g))
+        if acc + L > total:
+            if total - acc > 0:
+                out.append(total - acc)
+            return out
+        out.append(L)
+        acc += L
+
+
+def layer_kind(i: int) -> str:
+    """Layer i of the 22-layer schedule is global iff i % 3 == 0."""
+    return "global" if i % 3 == 0 else "local"
+
+
+def config(k: int, layer: int = 0) -> Workload:
+    """The five synthetic workloads.
+
+    1: one sequence of 300 tokens, sigma 1, seed 1.
+    2: 8 sequences, L ~ U{64..512}, sigma 1, seed 2.
+    3: one sequence of 8192 tokens, sigma 1, seed 3.
+    4: 65536 tokens, L ~ U{128..8192} filled to the total, sigma 0.5, seed 4.
+    5: 32 x 8192 tokens; layer i of 22 uses seed 1000 + i and is global iff
+       i % 3 == 0.
+    """
+    if k == 1:
+        g = torch.Generator().manual_seed(1)
+        lengths = [300]
+        sigma, kinds, seed = 1.0, ["local", "global"], 1
+    elif k == 2:
+        g = torch.Generator().manual_seed(2)
+        lengths = _uniform_lengths(g, 8, 64, 512)
+        sigma, kinds, seed = 1.0, ["local", "global"], 2
+    elif k == 3:
+        g = torch.Generator().manual_seed(3)
+        lengths = [8192]
+        sigma, kinds, seed = 1.0, ["global", "local"], 3
+    elif k == 4:
+        g = torch.Generator().manual_seed(4)
+        lengths = _fill_lengths(g, 65536, 128, 8192)
+        sigma, kinds, seed = 0.5, ["local", "global"], 4
+    elif k == 5:
+        seed = 1000 + layer
+        g = torch.Generator().manual_seed(seed)
+        lengths = [8192] * 32
+        sigma, kinds = 1.0, [layer_kind(layer)]
+    else:
+        raise ValueError(f"no workload {k}")
+    cu = cu_from_lengths(lengths)
+    qkv = draw_qkv(g, int(cu[-1]), sigma)
+    return Workload(f"config{k}" + (f"_layer{layer}" if k == 5 else ""), seed, sigma,
+                    lengths, kinds, qkv, cu)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """uint16 view of a bf16 CPU tensor (no conversion)."""
+    assert t.dtype == torch.bfloat16
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def sample_rows(cu_seqlens, per_seq: int, seed: int) -> np.ndarray:
+    """A seeded, sorted sample of packed row indices: `per_seq` rows from each
+    sequence (all of them when it is shorter), always including its first and
+    last rows."""
+    g = torch.Generator().manual_seed(seed)
+    cu = [int(x) for x in cu_seqlens]
+    rows = []
+    for s in range(len(cu) - 1):
+        b, e = cu[s], cu[s + 1]
+        L = e - b
+        if L <= 0:
+            continue
+        if L <= per_seq:
+            rows.extend(range(b, e))
+            continue
+        pick = torch.randperm(L, generator=g)[:per_seq - 2].tolist()
+        sel = set(pick) | {0, L - 1}
+        rows.extend(b + i for i in sorted(sel))
+    return np.asarray(sorted(rows), dtype=np.int64)

@@ -1,0 +1,157 @@
+"""fp64 CPU oracle for the ModernBERT-base attention block (ctypes binding).
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's
+CPU-baseline / reference legs may import this package.  The CUDA library never
+does, and this package imports nothing from it.
+
+What it computes is stated in mbert_attn_oracle.c with the passages it follows.
+Layer constants are restated here from the pages, independently of the CUDA
+path:
+
+* "ModernBERT-base Architecture Teardown", "How Does RoPE Work With Two
+  Bases?": base 160000 on global layers, 10000 on local layers.
+* same page, "What Are Local and Global Attention?" and "ModernBERT"
+  (candding), "The alternating attention": local layers keep |i - j| <= 64.
+* teardown, "How Does ModernBERT Make Q, K and V?": 12 heads of 64.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+HEADS = 12
+HEAD_DIM = 64
+GLOBAL = {"theta": 160000.0, "half_window": -1}
+LOCAL = {"theta": 10000.0, "half_window": 64}
+KINDS = {"global": GLOBAL, "local": LOCAL}
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        L.oracle_inv_freq.argtypes = [ctypes.c_double, ctypes.c_int, dp]
+        L.oracle_inv_freq.restype = None
+        L.oracle_rope_row.argtypes = [dp, ctypes.c_int64, ctypes.c_double, ctypes.c_int, dp]
+        L.oracle_rope_row.restype = None
+        L.oracle_key_counts.argtypes = [i32p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, i32p]
+        L.oracle_key_counts.restype = ctypes.c_int
+        L.oracle_sdpa_dense.argtypes = [dp, dp, dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_double, u8p, dp, dp]
+        L.oracle_sdpa_dense.restype = ctypes.c_int
+        L.oracle_attention.argtypes = [u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, i32p,
+                                       ctypes.c_int, ctypes.c_double, ctypes.c_int, i64p,
+                                       ctypes.c_int64, dp, i32p, ctypes.c_int]
+        L.oracle_attention.restype = ctypes.c_int
+        L.oracle_max_threads.argtypes = []
+        L.oracle_max_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
+
+
+def inv_freq(theta: float, head_dim: int = HEAD_DIM) -> np.ndarray:
+    out = np.empty(head_dim // 2, dtype=np.float64)
+    lib().oracle_inv_freq(float(theta), int(head_dim), _ptr(out, ctypes.c_double))
+    return out
+
+
+def rope(x, pos: int, theta: float) -> np.ndarray:
+    """Rotate one head row x[head_dim] (fp64) sitting at position `pos`."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    lib().oracle_rope_row(_ptr(x, ctypes.c_double), int(pos), float(theta), x.shape[0],
+                          _ptr(y, ctypes.c_double))
+    return y
+
+
+def key_counts(cu_seqlens, half_window: int) -> np.ndarray:
+    """|A_i| of every packed row, by brute force over the band predicate."""
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    T = int(cu[-1])
+    counts = np.zeros(T, dtype=np.int32)
+    rc = lib().oracle_key_counts(_ptr(cu, ctypes.c_int32), len(cu) - 1, T, int(half_window),
+                                 _ptr(counts, ctypes.c_int32))
+    if rc:
+        raise ValueError(f"oracle_key_counts: bad cu_seqlens (code {rc})")
+    return counts
+
+
+def sdpa_dense(Q, K, V, scale: float, mask=None):
+    """softmax(scale * Q K^T, masked) V in fp64.  Returns (weights, out)."""
+    Q = np.ascontiguousarray(Q, dtype=np.float64)
+    K = np.ascontiguousarray(K, dtype=np.float64)
+    V = np.ascontiguousarray(V, dtype=np.float64)
+    n, d = Q.shape
+    m, dv = V.shape
+    assert K.shape == (m, d)
+    w = np.empty((n, m), dtype=np.float64)
+    o = np.empty((n, dv), dtype=np.float64)
+    mp = None
+    if mask is not None:
+        mk = np.ascontiguousarray(mask, dtype=np.uint8)
+        assert mk.shape == (n, m)
+        mp = _ptr(mk, ctypes.c_uint8)
+    rc = lib().oracle_sdpa_dense(_ptr(Q, ctypes.c_double), _ptr(K, ctypes.c_double),
+                                 _ptr(V, ctypes.c_double), n, m, d, dv, float(scale), mp,
+                                 _ptr(w, ctypes.c_double), _ptr(o, ctypes.c_double))
+    if rc:
+        raise ValueError(f"oracle_sdpa_dense failed ({rc})")
+    return w, o
+
+
+def attention(qkv_bits, cu_seqlens, theta: float, half_window: int, rows=None,
+              threads: int = 0, heads: int = HEADS, head_dim: int = HEAD_DIM):
+    """The attention block in fp64.
+
+    qkv_bits: uint16 [T, 3*heads*head_dim], the bf16 bit patterns of the fused
+    Wqkv output.  cu_seqlens: int32 [n_seqs+1].  rows: None (every row) or a
+    sorted array of packed row indices.  Returns (out fp64 [n, heads*head_dim],
+    counts int32 [n]).
+    """
+    q = np.ascontiguousarray(qkv_bits)
+    if q.dtype != np.uint16:
+        raise TypeError("qkv_bits must be uint16 bf16 bit patterns")
+    T = q.shape[0]
+    assert q.shape[1] == 3 * heads * head_dim
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    if rows is None:
+        n = T
+        rp = None
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        n = r.shape[0]
+        rp = _ptr(r, ctypes.c_int64)
+    out = np.empty((n, heads * head_dim), dtype=np.float64)
+    counts = np.zeros(n, dtype=np.int32)
+    rc = lib().oracle_attention(_ptr(q, ctypes.c_uint16), T, heads, head_dim,
+                                _ptr(cu, ctypes.c_int32), len(cu) - 1, float(theta),
+                                int(half_window), rp, n, _ptr(out, ctypes.c_double),
+                                _ptr(counts, ctypes.c_int32), int(threads))
+    if rc:
+        raise ValueError(f"oracle_attention failed (code {rc})")
+    return out, counts
+
+
+def attention_kind(qkv_bits, cu_seqlens, kind: str, rows=None, threads: int = 0):
+    """attention() with the constants of a ModernBERT-base layer kind."""
+    p = KINDS[kind]
+    return attention(qkv_bits, cu_seqlens, p["theta"], p["half_window"], rows=rows,
+                     threads=threads)

@@ -1,0 +1,109 @@
+"""Planted mistakes: each plausible error, put into a copy of the oracle on
+the CPU, must make at least one pin of test_oracle.py fail.
+
+The copy is made by a textual edit of the oracle's C source, compiled into a
+temporary library and swapped in for the duration of the check; the oracle
+itself is never modified.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from oracle import build as obuild
+import test_oracle as T
+
+# (name, original source fragment, planted fragment)
+PLANTS = [
+    ("rope_sign", "y[m] = a * c - b * s;", "y[m] = a * c + b * s;"),
+    ("rope_interleaved_pairs", "double a = x[m], b = x[m + half];",
+     "double a = x[2 * m], b = x[2 * m + 1];"),
+    ("no_scale", "sc[j - j0] = acc * scale;", "sc[j - j0] = acc;"),
+    ("window_exclusive", "return d <= (int64_t)half_window;", "return d < (int64_t)half_window;"),
+    ("band_one_short", "hi = i + half_window + 1;", "hi = i + half_window;"),
+    ("positions_not_restarting", "const int64_t i = row - row0;  ", "const int64_t i = row;  "),
+    ("values_from_key_block", "+ 2 * c->heads * c->head_dim + c->h * c->head_dim;",
+     "+ c->heads * c->head_dim + c->h * c->head_dim;"),
+    ("softmax_without_max", "den += exp(scores[j] - m);", "den += exp(scores[j]);"),
+    ("freq_exponent", "inv_freq[m] = pow(theta, -2.0 * (double)m / (double)head_dim);",
+     "inv_freq[m] = pow(theta, -1.0 * (double)m / (double)head_dim);"),
+]
+
+
+def _pins():
+    """The pins, as zero-argument callables."""
+    table = T._read_table("key_counts.txt")
+    out = [
+        T.test_worked_example_weights_match_page,
+        T.test_dense_rows_sum_to_one_and_mask_zeroes,
+        T.test_inv_freq_matches_printed_values,
+        T.test_rope_matches_complex_multiplication,
+        T.test_rope_relative_position_and_norm,
+        T.test_key_counts_closed_form,
+        T.test_global_equals_band_covering_sequence,
+        T.test_offset_in_pack_does_not_matter,
+        T.test_length_one_sequence_returns_its_value,
+        T.test_unit_values_give_unit_outputs,
+    ]
+    out += [(lambda r=r: T.test_key_counts_match_pages(r)) for r in table]
+    for lengths in ([5, 64, 65], [130, 7, 200]):
+        for kind in ("global", "local"):
+            out.append(lambda lengths=lengths, kind=kind: T.test_attention_matches_bruteforce(lengths, kind))
+    return out
+
+
+def _compile_variant(tmp_path, original, planted):
+    src = open(obuild.SRC).read()
+    assert src.count(original) == 1, f"fragment not unique in the oracle: {original!r}"
+    path = tmp_path / "planted.c"
+    path.write_text(src.replace(original, planted))
+    lib = tmp_path / "libplanted.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-shared",
+                    "-fPIC", "-o", str(lib), str(path), "-lm"], check=True)
+    return str(lib)
+
+
+@pytest.mark.parametrize("name,original,planted", PLANTS, ids=[p[0] for p in PLANTS])
+def test_planted_mistake_fails_a_pin(tmp_path, name, original, planted):
+    good = oracle.lib()
+    libpath = _compile_variant(tmp_path, original, planted)
+    bad = ctypes.CDLL(libpath)
+    for fn in ("oracle_inv_freq", "oracle_rope_row", "oracle_key_counts",
+               "oracle_sdpa_dense", "oracle_attention", "oracle_max_threads"):
+        getattr(bad, fn).argtypes = getattr(good, fn).argtypes
+        getattr(bad, fn).restype = getattr(good, fn).restype
+    failed = []
+    oracle._lib = bad
+    try:
+        for pin in _pins():
+            try:
+                pin()
+            except (AssertionError, ValueError):
+                failed.append(pin)
+    finally:
+        oracle._lib = good
+    assert failed, f"planted mistake {name!r} passed every pin"
+
+
+def test_unplanted_copy_passes_every_pin(tmp_path):
+    """Control: the same machinery with no edit passes all pins."""
+    good = oracle.lib()
+    src = open(obuild.SRC).read()
+    path = tmp_path / "copy.c"
+    path.write_text(src)
+    lib = tmp_path / "libcopy.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-shared",
+                    "-fPIC", "-o", str(lib), str(path), "-lm"], check=True)
+    copy = ctypes.CDLL(str(lib))
+    for fn in ("oracle_inv_freq", "oracle_rope_row", "oracle_key_counts",
+               "oracle_sdpa_dense", "oracle_attention", "oracle_max_threads"):
+        getattr(copy, fn).argtypes = getattr(good, fn).argtypes
+        getattr(copy, fn).restype = getattr(good, fn).restype
+    oracle._lib = copy
+    try:
+        for pin in _pins():
+            pin()
+    finally:
+        oracle._lib = good
