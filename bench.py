@@ -1,0 +1,412 @@
+#!/usr/bin/env python3
+"""Benchmark of the ModernBERT-base attention block on GB300.
+
+One step = the whole hot path over one batch: a global layer and a local
+layer of the attention block over one packed batch (default: one sequence of
+8192 tokens, qkv [8192, 2304] bf16 ~ N(0, 1), seed 3).  `value` is tokens/s
+through that layer pair, all ranks together; the per-layer figures, the
+TFLOP/s and the roofline fractions are reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one process per GPU, each rank on its own copy of
+the batch (weak scaling, no collective on the data path; a barrier and a max
+over ranks of the timed region only).  `--impl reference` times the fp64 CPU
+oracle on a bounded sample of the same workload (rank 0 only).
+
+Inputs stay resident in HBM during the timed region; 6 rotating sets of
+input/output buffers (377 MB, about 3x the 129 MB L2) keep each step's reads
+out of L2.  The `e2e` figure goes through the public API with pinned host
+buffers and counts the host<->device copies.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from encoder_only_transformer_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attention tokens/s and TFLOP/s (local & global layer) at 8192 tok, % of roofline"
+UNIT = "tokens/s"
+HEADS, HEAD_DIM = 12, 64
+FLOP_PER_PAIR = 4 * HEAD_DIM * HEADS           # QK^T + PV, all heads: 3072
+BYTES_PER_TOKEN = (2304 + 768) * 2             # read qkv once, write out once
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+N_SETS = 6
+
+WORKLOADS = {
+    "config3": (3, "1 sequence x 8192 tokens, qkv [8192,2304] bf16 ~ N(0,1), seed 3"),
+    "config4": (4, "65536 tokens, L ~ U{128..8192} packed, qkv bf16 ~ N(0,0.5), seed 4"),
+}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def admitted_pairs(lengths, kind, half_window=64):
+    """Sum over rows of the admitted-set size per head: L^2 on a global
+    layer; on a local layer 129 L - 4160 for L >= 65 (L^2 below)."""
+    tot = 0
+    for L in lengths:
+        if kind == "global" or L <= half_window + 1:
+            tot += L * L
+        else:
+            # 2hw+1 keys per row, minus hw - i missing keys for row i < hw at
+            # each end of the sequence
+            tot += (2 * half_window + 1) * L - half_window * (half_window + 1)
+    return tot
+
+
+def work(lengths, kind):
+    T = sum(lengths)
+    return {"flops": FLOP_PER_PAIR * admitted_pairs(lengths, kind),
+            "bytes": BYTES_PER_TOKEN * T}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Max of a per-rank float over all ranks (the slowest rank's time)."""
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def whole_job_tokens_per_s(tokens_per_rank: int, world: int, max_ms: float) -> float:
+    """Weak scaling: every rank processes its own batch; the job's rate is
+    the tokens of all ranks over the slowest rank's time."""
+    return world * tokens_per_rank / (max_ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class Clocks:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device):
+        self.proc = None
+        self.ident = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.ident = str(device.index)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100", "-i", self.ident],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": "nvidia-smi unavailable"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out = self.proc.communicate(timeout=10)[0]
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out = self.proc.communicate()[0]
+        sm, mx, reasons = [], [], set()
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[3:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"error": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def time_oracle(wl, rows_global, rows_local, seed=0):
+    """Seconds per query row (all 12 heads) of the fp64 oracle, per kind."""
+    import oracle
+    bits = W.bf16_bits(wl.qkv)
+    cu = wl.cu_seqlens.numpy()
+    out = {}
+    for kind, n in (("global", rows_global), ("local", rows_local)):
+        per_seq = max(2, n // max(1, wl.n_seqs))
+        rows = W.sample_rows(wl.cu_seqlens, per_seq, seed + (kind == "local"))
+        t0 = time.perf_counter()
+        oracle.attention_kind(bits, cu, kind, rows=rows)
+        out[kind] = ((time.perf_counter() - t0) / len(rows), len(rows))
+    return out, oracle.max_threads()
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    """The oracle as it stands, on a sample sized to ~budget_s of CPU work,
+    extrapolated to tokens/s through one global + one local layer."""
+    probe, cores = time_oracle(wl, 16, 128)
+    share = budget_s / 2
+    ng = int(min(wl.T, max(16, share / max(probe["global"][0], 1e-9))))
+    nl = int(min(wl.T, max(128, share / max(probe["local"][0], 1e-9))))
+    per_row, cores = time_oracle(wl, ng, nl, seed=1)
+    sec_per_token = per_row["global"][0] + per_row["local"][0]
+    return {"value": 1.0 / sec_per_token, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"fp64 oracle, {per_row['global'][1]} sampled query rows of the global "
+                       f"layer and {per_row['local'][1]} of the local layer (all 12 heads), "
+                       f"time per row extrapolated to {wl.T} tokens")}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch.distributed as dist
+    from encoder_only_transformer_gb300 import binding
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg_id, desc = WORKLOADS[args.workload]
+    wl = W.config(cfg_id)
+    T, L = wl.T, wl.max_seqlen
+    attn = binding.Attention(dev.index)
+    attn.reserve(T, wl.n_seqs)
+    cu = wl.cu_seqlens.to(dev)
+    qkv_sets = [wl.qkv.to(dev) for _ in range(N_SETS)]
+    out_sets = [(torch.empty(T, 768, dtype=torch.bfloat16, device=dev),
+                 torch.empty(T, 768, dtype=torch.bfloat16, device=dev)) for _ in range(N_SETS)]
+
+    def step(i, kinds=("global", "local")):
+        q = qkv_sets[i % N_SETS]
+        og, ol = out_sets[i % N_SETS]
+        for kind in kinds:
+            attn.forward(q, cu, kind, max_seqlen=L, out=og if kind == "global" else ol)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if attn.get_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # --- the timed region: K steps, with event pairs around each attention kernel
+    clocks = Clocks(dev)
+    attn.profile(True)
+    attn.profile_read()
+    barrier()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(i)
+    e1.record()
+    barrier()
+    clock_rec = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    kern_ms, kern_n, launches = attn.profile_read()
+    attn.profile(False)
+    if attn.get_error() != 0:
+        raise RuntimeError("device error in the timed region")
+
+    # --- per layer kind: the whole call (all its kernels), timed alone
+    per_kind = {}
+    kk = max(3, args.steps // 2)
+    for kind in ("global", "local"):
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(kk):
+            step(i, (kind,))
+        b.record()
+        barrier()
+        per_kind[kind] = max_over_ranks(a.elapsed_time(b), world, dev) / kk
+
+    # --- end to end through the public API, pinned host buffers
+    host_in = [wl.qkv.pin_memory(), wl.qkv.clone().pin_memory()]
+    host_out = [torch.empty(T, 768, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dev_in = [torch.empty_like(qkv_sets[0]) for _ in range(2)]
+
+    def e2e_step():
+        for j, kind in enumerate(("global", "local")):
+            dev_in[j].copy_(host_in[j], non_blocking=True)
+            o = binding.attention(dev_in[j], cu, kind, max_seqlen=L, out=out_sets[0][j])
+            host_out[j].copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    ke = max(3, args.steps // 4)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(ke):
+        e2e_step()
+    b.record()
+    barrier()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev) / ke
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    peaks, src = load_peaks()
+    ms_step = ms / args.steps
+    layers = {}
+    for kind in ("global", "local"):
+        wk = work(wl.lengths, kind)
+        t_kernel = kern_ms[kind] / max(1, kern_n[kind]) / 1e3
+        t_call = per_kind[kind] / 1e3
+        roof_t = max(wk["flops"] / (peaks["bf16_tflops"] * 1e12), wk["bytes"] / (peaks["hbm_gbs"] * 1e9))
+        layers[kind] = {
+            "tokens_per_s": T / t_call,
+            "ms_per_call": per_kind[kind],
+            "attn_kernel_ms": t_kernel * 1e3,
+            "tflops": wk["flops"] / t_kernel / 1e12,
+            "hbm_gbs": wk["bytes"] / t_kernel / 1e9,
+            "bound": "tensor" if wk["flops"] / (peaks["bf16_tflops"] * 1e12) >= wk["bytes"] / (peaks["hbm_gbs"] * 1e9) else "hbm",
+            "roofline_frac_kernel": roof_t / t_kernel,
+            "roofline_frac_call": roof_t / t_call,
+            "gflop": wk["flops"] / 1e9,
+            "mbytes": wk["bytes"] / 1e6,
+        }
+    g = layers["global"]
+    roofline = {"bound": "tensor", "achieved": g["tflops"], "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": g["tflops"] / peaks["bf16_tflops"], "traffic": None,
+                "kernel": "attn_generic_kernel (global layer)",
+                "peak_source": f"{src} bf16_tflops (burst)"}
+    rec = {
+        "metric": METRIC,
+        "value": whole_job_tokens_per_s(T, world, ms_step),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {desc}; step = 1 global + 1 local layer",
+                   "tokens_per_step_per_gpu": T, "n_seqs": wl.n_seqs,
+                   "l2": f"{N_SETS} rotating input/output buffer sets (inputs > L2 across steps)",
+                   "parallelism": f"{world} independent replica(s), no collective"},
+        "layers": layers,
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "clocks": clock_rec,
+        "e2e": {"value": whole_job_tokens_per_s(T, world, e2e_ms), "unit": UNIT,
+                "h2d_bytes_per_step": 2 * T * 2304 * 2, "d2h_bytes_per_step": 2 * T * 768 * 2},
+    }
+    if not args.no_cpu_baseline:
+        rec["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
+    if world > 1:
+        dist.destroy_process_group()
+    return rec
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    cfg_id, desc = WORKLOADS[args.workload]
+    wl = W.config(cfg_id)
+    probe, cores = time_oracle(wl, 16, 128)
+    # each step: a sample sized so that warm-up + steps take ~args.cpu_budget * 8 s in all
+    per_step = max(0.05, args.cpu_budget * 8 / max(1, args.steps + args.warmup))
+    ng = int(min(wl.T, max(2, per_step / 2 / max(probe["global"][0], 1e-9))))
+    nl = int(min(wl.T, max(2, per_step / 2 / max(probe["local"][0], 1e-9))))
+    for i in range(args.warmup):
+        time_oracle(wl, ng, nl, seed=100 + i)
+    secs = 0.0
+    rows = None
+    for i in range(args.steps):
+        r, cores = time_oracle(wl, ng, nl, seed=1000 + i)
+        secs += r["global"][0] + r["local"][0]
+        rows = (r["global"][1], r["local"][1])
+    sec_per_token = secs / args.steps
+    value = 1.0 / sec_per_token
+    sample = (f"fp64 oracle, per step {rows[0]} sampled query rows of the global layer and "
+              f"{rows[1]} of the local layer (all 12 heads), extrapolated to {wl.T} tokens")
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * sec_per_token * wl.T,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{args.workload}: {desc}; step = 1 global + 1 local layer",
+                   "tokens_per_step_per_gpu": wl.T},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="config3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rec = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if rec is not None:
+        print(json.dumps(rec), flush=True)
+
+
+if __name__ == "__main__":
+    main()

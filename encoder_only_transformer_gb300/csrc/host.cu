@@ -1,0 +1,465 @@
+// Host side of the mbert_attn C ABI: argument checks, the handle's device
+// memory (RoPE tables, work list, rotated-operand scratch, error word),
+// tensor-map encoding and kernel launches.
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "mbert_attn.h"
+#include "common.cuh"
+#include "internal.h"
+
+#define MBERT_API extern "C" __attribute__((visibility("default")))
+
+using namespace mbert;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct mbert_attn {
+    int device = 0;
+    int num_sms = 0;
+    mbert_attn_config cfg{};
+    float2 *rope[2] = {nullptr, nullptr};   // [MBERT_GLOBAL], [MBERT_LOCAL]: [max_seqlen][32]
+    int32_t *err = nullptr;                 // sticky device error word
+    int32_t *work_count = nullptr;
+    int2 *work = nullptr;
+    int64_t work_cap = 0;                   // entries
+    __nv_bfloat16 *rot = nullptr;           // rotated Q/K scratch [rows][1536]
+    int64_t rot_cap = 0;                    // rows
+    cudaStream_t last_stream = nullptr;
+    EncodeTiledFn encode = nullptr;
+    // measurement: event pairs around the attention kernel, per layer kind
+    bool profiling = false;
+    std::vector<cudaEvent_t> ev[2];         // start, end, start, end, ...
+    size_t ev_used[2] = {0, 0};
+    int64_t launches = 0;                   // every kernel this handle enqueued
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+            changed = cudaSetDevice(dev) == cudaSuccess;
+        }
+    }
+    ~DeviceGuard()
+    {
+        if (changed)
+            cudaSetDevice(prev);
+    }
+};
+
+int fail_cuda(cudaError_t e)
+{
+    (void)e;
+    return MBERT_ERR_CUDA;
+}
+
+// Upper bound on the number of (sequence, 128-query block) entries:
+// sum ceil(L/128) <= (T + 127 n) / 128.
+int64_t entry_bound(int64_t T, int64_t n)
+{
+    return (T + (kBlockM - 1) * n) / kBlockM;
+}
+
+int grow_workspace(mbert_attn *h, int64_t entries, int64_t rot_rows)
+{
+    if (entries > h->work_cap) {
+        int64_t cap = entries < 1024 ? 1024 : entries;
+        int2 *w = nullptr;
+        if (cudaMalloc(&w, sizeof(int2) * cap) != cudaSuccess) {
+            cudaGetLastError();
+            return MBERT_ERR_OOM;
+        }
+        if (h->work) {
+            cudaDeviceSynchronize();
+            cudaFree(h->work);
+        }
+        h->work = w;
+        h->work_cap = cap;
+    }
+    if (rot_rows > h->rot_cap) {
+        int64_t cap = rot_rows < 8192 ? 8192 : rot_rows;
+        __nv_bfloat16 *r = nullptr;
+        if (cudaMalloc(&r, sizeof(__nv_bfloat16) * 2 * kHidden * cap) != cudaSuccess) {
+            cudaGetLastError();
+            return MBERT_ERR_OOM;
+        }
+        if (h->rot) {
+            cudaDeviceSynchronize();
+            cudaFree(h->rot);
+        }
+        h->rot = r;
+        h->rot_cap = cap;
+    }
+    return MBERT_OK;
+}
+
+// 2-D bf16 tensor map over [rows][width] (row pitch = width * 2 bytes),
+// box 64 columns x 128 rows, 128-byte swizzle, out-of-range reads give 0.
+int encode_map(mbert_attn *h, CUtensorMap *tm, const void *ptr, int width, int64_t rows)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(width) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(kBlockM)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = h->encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MBERT_OK : MBERT_ERR_CUDA;
+}
+
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+// Common argument checks of forward / key_counts.
+int check_common(const mbert_attn *h, const int32_t *cu, int n_seqs, int64_t T, int max_seqlen,
+                 int layer_kind)
+{
+    if (!h)
+        return MBERT_ERR_BAD_ARG;
+    if (n_seqs < 0 || T < 0 || T > INT32_MAX || max_seqlen < 0)
+        return MBERT_ERR_BAD_ARG;
+    if (layer_kind != MBERT_GLOBAL && layer_kind != MBERT_LOCAL)
+        return MBERT_ERR_BAD_ARG;
+    if (T > 0 && (n_seqs == 0 || !cu))
+        return MBERT_ERR_BAD_ARG;
+    if (max_seqlen > h->cfg.max_seqlen)
+        return MBERT_ERR_SEQ_TOO_LONG;
+    return MBERT_OK;
+}
+
+Plan make_plan(mbert_attn *h, const int32_t *cu, int n_seqs, int64_t T, int max_seqlen)
+{
+    Plan p;
+    p.cu = cu;
+    p.n_seqs = n_seqs;
+    p.T = T;
+    p.max_seqlen = max_seqlen > 0 ? max_seqlen : h->cfg.max_seqlen;
+    p.work = h->work;
+    p.work_count = h->work_count;
+    p.entry_bound = static_cast<int>(entry_bound(T, n_seqs));
+    p.err = h->err;
+    return p;
+}
+
+}  // namespace
+
+MBERT_API int mbert_attn_default_config(mbert_attn_config *cfg)
+{
+    if (!cfg)
+        return MBERT_ERR_BAD_ARG;
+    cfg->heads = kHeads;
+    cfg->head_dim = kHeadDim;
+    cfg->half_window = 64;
+    cfg->max_seqlen = 8192;
+    cfg->theta_global = 160000.0;
+    cfg->theta_local = 10000.0;
+    return MBERT_OK;
+}
+
+MBERT_API const char *mbert_attn_strerror(int status)
+{
+    switch (status) {
+    case MBERT_OK: return "success";
+    case MBERT_ERR_BAD_ARG: return "invalid argument";
+    case MBERT_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case MBERT_ERR_SEQ_TOO_LONG: return "sequence longer than max_seqlen";
+    case MBERT_ERR_BAD_CU_SEQLENS: return "invalid cu_seqlens";
+    case MBERT_ERR_TIMEOUT: return "device wait timed out";
+    case MBERT_ERR_CUDA: return "CUDA runtime error";
+    case MBERT_ERR_OOM: return "out of device memory";
+    default: return "unknown status";
+    }
+}
+
+MBERT_API void mbert_attn_destroy(mbert_attn *h)
+{
+    if (!h)
+        return;
+    {
+        DeviceGuard g(h->device);
+        for (int k = 0; k < 2; ++k)
+            for (cudaEvent_t e : h->ev[k])
+                cudaEventDestroy(e);
+        cudaFree(h->rope[0]);
+        cudaFree(h->rope[1]);
+        cudaFree(h->err);
+        cudaFree(h->work_count);
+        cudaFree(h->work);
+        cudaFree(h->rot);
+    }
+    delete h;
+}
+
+MBERT_API int mbert_attn_create(mbert_attn **out, const mbert_attn_config *cfg, int device)
+{
+    if (!out)
+        return MBERT_ERR_BAD_ARG;
+    *out = nullptr;
+    mbert_attn_config c;
+    if (cfg)
+        c = *cfg;
+    else
+        mbert_attn_default_config(&c);
+    if (c.heads != kHeads || c.head_dim != kHeadDim)
+        return MBERT_ERR_UNSUPPORTED;
+    if (c.half_window < 0 || c.half_window > 128 || c.max_seqlen < 1 ||
+        c.max_seqlen > 1024 * kBlockM || !(c.theta_global > 1.0) || !(c.theta_local > 1.0))
+        return MBERT_ERR_BAD_ARG;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+        cudaGetLastError();
+        return MBERT_ERR_UNSUPPORTED;
+    }
+    if (device < 0 || device >= ndev)
+        return MBERT_ERR_BAD_ARG;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess)
+        return MBERT_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3)
+        return MBERT_ERR_UNSUPPORTED;   // the kernels are built for sm_103a only
+
+    mbert_attn *h = new (std::nothrow) mbert_attn;
+    if (!h)
+        return MBERT_ERR_OOM;
+    h->device = device;
+    h->num_sms = prop.multiProcessorCount;
+    h->cfg = c;
+    DeviceGuard g(device);
+
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q)
+            != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        delete h;
+        return MBERT_ERR_CUDA;
+    }
+    h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+
+    // RoPE tables: cos and sin of pos * base^(-2m/64), evaluated in fp64 and
+    // stored as fp32 ("ModernBERT-base Architecture Teardown", "How Does
+    // RoPE Work With Two Bases?"; "ModernBERT" (candding), "The two rope
+    // tables": both tables are built once, up to the longest sequence).
+    const size_t n = static_cast<size_t>(c.max_seqlen) * kPairs;
+    float2 *host = static_cast<float2 *>(std::malloc(sizeof(float2) * n));
+    if (!host) {
+        delete h;
+        return MBERT_ERR_OOM;
+    }
+    int rc = MBERT_OK;
+    const double thetas[2] = {c.theta_global, c.theta_local};
+    for (int k = 0; k < 2 && rc == MBERT_OK; ++k) {
+        double inv[kPairs];
+        for (int m = 0; m < kPairs; ++m)
+            inv[m] = std::pow(thetas[k], -2.0 * m / kHeadDim);
+        for (int p = 0; p < c.max_seqlen; ++p)
+            for (int m = 0; m < kPairs; ++m) {
+                const double a = static_cast<double>(p) * inv[m];
+                host[static_cast<size_t>(p) * kPairs + m] =
+                    make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+            }
+        if (cudaMalloc(&h->rope[k], sizeof(float2) * n) != cudaSuccess)
+            rc = MBERT_ERR_OOM;
+        else if (cudaMemcpy(h->rope[k], host, sizeof(float2) * n, cudaMemcpyHostToDevice) != cudaSuccess)
+            rc = MBERT_ERR_CUDA;
+    }
+    std::free(host);
+    if (rc == MBERT_OK) {
+        if (cudaMalloc(&h->err, sizeof(int32_t)) != cudaSuccess ||
+            cudaMalloc(&h->work_count, sizeof(int32_t)) != cudaSuccess)
+            rc = MBERT_ERR_OOM;
+        else if (cudaMemset(h->err, 0, sizeof(int32_t)) != cudaSuccess ||
+                 cudaMemset(h->work_count, 0, sizeof(int32_t)) != cudaSuccess)
+            rc = MBERT_ERR_CUDA;
+    }
+    if (rc == MBERT_OK)
+        rc = grow_workspace(h, entry_bound(c.max_seqlen, 1), 0);
+    if (rc != MBERT_OK) {
+        cudaGetLastError();
+        mbert_attn_destroy(h);
+        return rc;
+    }
+    *out = h;
+    return MBERT_OK;
+}
+
+MBERT_API int mbert_attn_reserve(mbert_attn *h, int64_t max_tokens, int64_t max_seqs)
+{
+    if (!h || max_tokens < 0 || max_seqs < 0 || max_tokens > INT32_MAX)
+        return MBERT_ERR_BAD_ARG;
+    DeviceGuard g(h->device);
+    return grow_workspace(h, entry_bound(max_tokens, max_seqs), max_tokens);
+}
+
+MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *cu_seqlens,
+                                 int n_seqs, int64_t total_tokens, int max_seqlen,
+                                 int layer_kind, void *out, void *stream)
+{
+    int rc = check_common(h, cu_seqlens, n_seqs, total_tokens, max_seqlen, layer_kind);
+    if (rc != MBERT_OK)
+        return rc;
+    const int64_t T = total_tokens;
+    if (T == 0)
+        return MBERT_OK;
+    if (!qkv || !out)
+        return MBERT_ERR_BAD_ARG;
+    if ((reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+        return MBERT_ERR_BAD_ARG;
+    if (ranges_overlap(qkv, static_cast<size_t>(T) * kQKVWidth * 2, out,
+                       static_cast<size_t>(T) * kHidden * 2))
+        return MBERT_ERR_BAD_ARG;
+
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = grow_workspace(h, entry_bound(T, n_seqs), T);
+    if (rc != MBERT_OK)
+        return rc;
+    Plan p = make_plan(h, cu_seqlens, n_seqs, T, max_seqlen);
+
+    AttnArgs a;
+    if (encode_map(h, &a.tm_rot, h->rot, 2 * kHidden, T) != MBERT_OK ||
+        encode_map(h, &a.tm_qkv, qkv, kQKVWidth, T) != MBERT_OK)
+        return MBERT_ERR_CUDA;
+    a.cu = cu_seqlens;
+    a.work = h->work;
+    a.work_count = h->work_count;
+    a.entry_bound = p.entry_bound;
+    a.half_window = layer_kind == MBERT_GLOBAL ? -1 : h->cfg.half_window;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.err = h->err;
+
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    if (h->profiling) {
+        std::vector<cudaEvent_t> &v = h->ev[layer_kind];
+        while (v.size() < h->ev_used[layer_kind] + 2) {
+            cudaEvent_t x;
+            if (cudaEventCreate(&x) != cudaSuccess)
+                return MBERT_ERR_CUDA;
+            v.push_back(x);
+        }
+        ev0 = v[h->ev_used[layer_kind]];
+        ev1 = v[h->ev_used[layer_kind] + 1];
+        h->ev_used[layer_kind] += 2;
+    }
+    cudaError_t e = launch_plan(p, st);
+    if (e == cudaSuccess)
+        e = launch_rope_qk(p, static_cast<const __nv_bfloat16 *>(qkv), h->rope[layer_kind],
+                           h->cfg.max_seqlen, h->rot, st);
+    if (e == cudaSuccess && ev0)
+        e = cudaEventRecord(ev0, st);
+    if (e == cudaSuccess)
+        e = launch_attn_generic(a, st);
+    if (e == cudaSuccess && ev1)
+        e = cudaEventRecord(ev1, st);
+    h->launches += 3;
+    h->last_stream = st;
+    return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
+}
+
+MBERT_API int mbert_attn_key_counts(mbert_attn *h, const int32_t *cu_seqlens, int n_seqs,
+                                    int64_t total_tokens, int max_seqlen, int layer_kind,
+                                    int32_t *counts, void *stream)
+{
+    int rc = check_common(h, cu_seqlens, n_seqs, total_tokens, max_seqlen, layer_kind);
+    if (rc != MBERT_OK)
+        return rc;
+    if (total_tokens == 0)
+        return MBERT_OK;
+    if (!counts)
+        return MBERT_ERR_BAD_ARG;
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = grow_workspace(h, entry_bound(total_tokens, n_seqs), 0);
+    if (rc != MBERT_OK)
+        return rc;
+    Plan p = make_plan(h, cu_seqlens, n_seqs, total_tokens, max_seqlen);
+    h->launches += 2;
+    cudaError_t e = launch_plan(p, st);
+    if (e == cudaSuccess)
+        e = launch_key_count(p, layer_kind == MBERT_GLOBAL ? -1 : h->cfg.half_window, counts, st);
+    h->last_stream = st;
+    return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
+}
+
+MBERT_API int mbert_attn_get_error(mbert_attn *h)
+{
+    if (!h)
+        return MBERT_ERR_BAD_ARG;
+    DeviceGuard g(h->device);
+    if (cudaStreamSynchronize(h->last_stream) != cudaSuccess)
+        return MBERT_ERR_CUDA;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, h->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(h->err, 0, sizeof(int32_t)) != cudaSuccess)
+        return MBERT_ERR_CUDA;
+    if (word & kErrTimeout)
+        return MBERT_ERR_TIMEOUT;
+    if (word & kErrBadCu)
+        return MBERT_ERR_BAD_CU_SEQLENS;
+    if (word & kErrTooLong)
+        return MBERT_ERR_SEQ_TOO_LONG;
+    return MBERT_OK;
+}
+
+MBERT_API int mbert_attn_selftest_timeout(mbert_attn *h, int64_t limit_us, void *stream)
+{
+    if (!h || limit_us <= 0 || limit_us > 2000000)
+        return MBERT_ERR_BAD_ARG;
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_wait_timeout_selftest(
+        h->err, static_cast<unsigned long long>(limit_us) * 1000ull, st);
+    h->last_stream = st;
+    return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
+}
+
+MBERT_API int mbert_attn_profile_enable(mbert_attn *h, int enable)
+{
+    if (!h)
+        return MBERT_ERR_BAD_ARG;
+    h->profiling = enable != 0;
+    return MBERT_OK;
+}
+
+MBERT_API int mbert_attn_profile_read(mbert_attn *h, double *attn_ms, int64_t *attn_launches,
+                                      int64_t *total_launches)
+{
+    if (!h)
+        return MBERT_ERR_BAD_ARG;
+    DeviceGuard g(h->device);
+    for (int k = 0; k < 2; ++k) {
+        double ms = 0.0;
+        for (size_t i = 0; i + 1 < h->ev_used[k]; i += 2) {
+            float x = 0.f;
+            if (cudaEventSynchronize(h->ev[k][i + 1]) != cudaSuccess ||
+                cudaEventElapsedTime(&x, h->ev[k][i], h->ev[k][i + 1]) != cudaSuccess)
+                return MBERT_ERR_CUDA;
+            ms += x;
+        }
+        if (attn_ms)
+            attn_ms[k] = ms;
+        if (attn_launches)
+            attn_launches[k] = static_cast<int64_t>(h->ev_used[k] / 2);
+        h->ev_used[k] = 0;
+    }
+    if (total_launches)
+        *total_launches = h->launches;
+    h->launches = 0;
+    return MBERT_OK;
+}

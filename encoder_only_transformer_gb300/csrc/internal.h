@@ -1,0 +1,55 @@
+// Launch interface between the host library (host.cu) and the kernel
+// translation units.  Not part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace mbert {
+
+// Work list written by the plan kernel: one entry per (sequence, 128-query
+// block), longest sequences first; the attention grid covers entries x heads.
+struct Plan {
+    const int32_t *cu;      // device [n_seqs + 1]
+    int n_seqs;
+    int64_t T;
+    int max_seqlen;         // longest sequence accepted by the device check
+    int2 *work;             // device [entry_bound]
+    int32_t *work_count;    // device scalar: entries written (0 if the checks failed)
+    int entry_bound;        // host-side upper bound on the entry count
+    int32_t *err;           // device error word (sticky, bit mask)
+};
+
+cudaError_t launch_plan(const Plan &p, cudaStream_t stream);
+
+// Rotate Q and K of every row (all heads) into rot[T][1536] bf16.
+cudaError_t launch_rope_qk(const Plan &p, const __nv_bfloat16 *qkv, const float2 *table,
+                           int table_rows, __nv_bfloat16 *rot, cudaStream_t stream);
+
+// Admitted-key count per query row, from the attention kernels' tile
+// schedule and mask.
+cudaError_t launch_key_count(const Plan &p, int half_window, int32_t *counts,
+                             cudaStream_t stream);
+
+struct AttnArgs {
+    CUtensorMap tm_rot;     // rotated Q/K [T][1536], box 64 x 128, 128B swizzle
+    CUtensorMap tm_qkv;     // qkv [T][2304], box 64 x 128, 128B swizzle
+    const int32_t *cu;
+    const int2 *work;
+    const int32_t *work_count;
+    int entry_bound;
+    int half_window;        // < 0: global layer
+    __nv_bfloat16 *out;     // [T][768]
+    int32_t *err;
+};
+
+// One bounded mbarrier wait that nothing completes (exercises kErrTimeout).
+cudaError_t launch_wait_timeout_selftest(int32_t *err, unsigned long long limit_ns,
+                                         cudaStream_t stream);
+
+// Generic flash attention over pre-rotated Q/K: one CTA per (entry, head).
+cudaError_t launch_attn_generic(const AttnArgs &a, cudaStream_t stream);
+
+}  // namespace mbert

@@ -1,0 +1,161 @@
+/*
+ * mbert_attn: the bidirectional self-attention block of ModernBERT-base as a
+ * C-ABI library for NVIDIA GB300 (sm_103a).
+ *
+ * What one call computes (page title, section):
+ *  - Input: the fused Wqkv output, one row of 2304 bf16 numbers per token,
+ *    cut as (3, 12, 64): columns 0..767 are Q, 768..1535 K, 1536..2303 V,
+ *    head h at columns h*64 .. h*64+63 of each block ("ModernBERT-base
+ *    Architecture Teardown", "How Does ModernBERT Make Q, K and V?";
+ *    "ModernBERT" (candding), "The tensors").
+ *  - RoPE, rotate-half over the full 64-wide head, on Q and K only; pair m
+ *    turns by pos * base^(-2m/64); base 160000 on global layers, 10000 on
+ *    local layers (teardown, "How Does RoPE Work With Two Bases?"; candding,
+ *    "The two rope tables").  Positions restart at 0 in every sequence.
+ *  - Scores q.k / sqrt(64), softmax along the keys, weighted blend of V, no
+ *    causal mask (teardown, "How Does Self-Attention Work?").
+ *  - Local layers keep key j for query i when |i - j| <= 64; global layers
+ *    keep every key of the sequence (teardown, "What Are Local and Global
+ *    Attention?"; candding, "The alternating attention").
+ *  - Sequences are unpadded and packed back to back; cu_seqlens holds their
+ *    offsets.  A query never sees keys of another sequence, which is what a
+ *    padding mask achieves for a padded batch ("Encoder-only models"
+ *    (rayaq), padding mask; teardown, "What Is ModernBERT-base?", unpadding).
+ *  - Output: out[t, h*64 + d], 768 bf16 per token, heads in input order,
+ *    ready for Wo (teardown, "How Does ModernBERT Make Q, K and V?").
+ *
+ * Conventions for every entry point:
+ *  - Status: 0 on success, a negative MBERT_ERR_* code otherwise.  Host-side
+ *    argument checks are synchronous and enqueue nothing when they fail.
+ *    Checks that need device data (cu_seqlens contents) run on the GPU and
+ *    are reported later by mbert_attn_get_error().
+ *  - Pointers marked "device" must be CUDA device (or managed) memory on the
+ *    handle's device; "host" pointers are ordinary host memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  All device work is enqueued asynchronously on it; the caller
+ *    keeps ownership of the stream and of every buffer it passes.
+ *  - A handle may be used from one host thread at a time.
+ */
+#ifndef MBERT_ATTN_H
+#define MBERT_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque handle: owns the two RoPE cos/sin tables, the device work-list
+ * workspace, the rotated-operand scratch and the device error word. */
+typedef struct mbert_attn mbert_attn;
+
+/* Layer kinds.  Layer i of the 22-layer stack is global iff i % 3 == 0
+ * (teardown, "What Are Local and Global Attention?"). */
+enum {
+    MBERT_GLOBAL = 0,
+    MBERT_LOCAL = 1
+};
+
+/* Status codes. */
+enum {
+    MBERT_OK = 0,
+    MBERT_ERR_BAD_ARG = -1,        /* null/misaligned/aliased pointer, bad size or kind */
+    MBERT_ERR_UNSUPPORTED = -2,    /* config other than 12 heads x 64, or no sm_103 device */
+    MBERT_ERR_SEQ_TOO_LONG = -3,   /* a sequence longer than the handle's max_seqlen */
+    MBERT_ERR_BAD_CU_SEQLENS = -4, /* cu_seqlens[0] != 0, decreasing, or cu[n] != T (device-detected) */
+    MBERT_ERR_TIMEOUT = -5,        /* a kernel's bounded wait ran out; results are invalid */
+    MBERT_ERR_CUDA = -6,           /* a CUDA runtime call failed */
+    MBERT_ERR_OOM = -7             /* device allocation failed */
+};
+
+/* Create-time configuration. */
+typedef struct {
+    int heads;            /* must be 12 */
+    int head_dim;         /* must be 64 */
+    int half_window;      /* local band half-width, |i - j| <= half_window (64), 0..128 */
+    int max_seqlen;       /* longest sequence accepted; sizes the RoPE tables (8192) */
+    double theta_global;  /* RoPE base of global layers (160000) */
+    double theta_local;   /* RoPE base of local layers (10000) */
+} mbert_attn_config;
+
+/* Fill *cfg with ModernBERT-base's values: 12, 64, 64, 8192, 160000, 10000. */
+int mbert_attn_default_config(mbert_attn_config *cfg);
+
+/* Create a handle on CUDA device `device` (host pointer out, host pointer
+ * cfg; cfg == NULL means the defaults).  Allocates the RoPE tables
+ * (2 x max_seqlen x 32 x (cos, sin) fp32, computed in fp64 on the host) and a
+ * small workspace.  Synchronous.  On failure *out is NULL. */
+int mbert_attn_create(mbert_attn **out, const mbert_attn_config *cfg, int device);
+
+/* Grow the workspace so that later forward calls with up to `max_tokens`
+ * packed tokens in up to `max_seqs` sequences allocate nothing.  Optional:
+ * mbert_attn_forward grows it on demand (a synchronous cudaMalloc). */
+int mbert_attn_reserve(mbert_attn *h, int64_t max_tokens, int64_t max_seqs);
+
+/* The attention block for one layer.
+ *   qkv          device, bf16 [total_tokens][2304] row-major, 16-byte aligned.
+ *   cu_seqlens   device, int32 [n_seqs + 1]; cu[0] = 0, non-decreasing,
+ *                cu[n_seqs] = total_tokens.  Empty sequences are allowed.
+ *   n_seqs       >= 0; total_tokens >= 0 (0 enqueues nothing).
+ *   max_seqlen   caller's bound on the longest sequence (<= the handle's
+ *                max_seqlen, else MBERT_ERR_SEQ_TOO_LONG); a longer sequence
+ *                found on the device sets MBERT_ERR_SEQ_TOO_LONG.
+ *   layer_kind   MBERT_GLOBAL or MBERT_LOCAL.
+ *   out          device, bf16 [total_tokens][768], 16-byte aligned, must not
+ *                overlap qkv.  Every row of every sequence is written.
+ * Enqueues a few kernels on `stream`; when the device-side checks fail the
+ * attention kernels write nothing and the error is reported by
+ * mbert_attn_get_error(). */
+int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *cu_seqlens,
+                       int n_seqs, int64_t total_tokens, int max_seqlen,
+                       int layer_kind, void *out, void *stream);
+
+/* Debug/verification entry: for every packed row, the number of keys the
+ * attention kernel's tile schedule and mask admit for that query (the size
+ * of its admitted set), computed by the same device code the forward pass
+ * uses to choose and mask key tiles.  counts: device int32 [total_tokens].
+ * Other arguments as for mbert_attn_forward. */
+int mbert_attn_key_counts(mbert_attn *h, const int32_t *cu_seqlens, int n_seqs,
+                          int64_t total_tokens, int max_seqlen, int layer_kind,
+                          int32_t *counts, void *stream);
+
+/* Wait for the handle's most recent stream, then return (and clear) the
+ * device error word as a status: MBERT_OK, MBERT_ERR_BAD_CU_SEQLENS,
+ * MBERT_ERR_SEQ_TOO_LONG or MBERT_ERR_TIMEOUT; MBERT_ERR_CUDA if the wait
+ * itself fails. */
+int mbert_attn_get_error(mbert_attn *h);
+
+/* Diagnostic: enqueue one kernel whose bounded wait on a barrier that
+ * nothing completes gives up after limit_us microseconds (1 .. 2000000),
+ * exactly as the attention kernels' waits do if a transfer or an MMA never
+ * completes.  Afterwards mbert_attn_get_error() returns MBERT_ERR_TIMEOUT.
+ * Nothing faults or traps; the context stays usable. */
+int mbert_attn_selftest_timeout(mbert_attn *h, int64_t limit_us, void *stream);
+
+/* Measurement.  While enabled, every mbert_attn_forward also records a
+ * CUDA event pair on its stream around its attention kernel (the plan and
+ * RoPE kernels before it are outside the pair).  The handle always counts
+ * the kernels it enqueues. */
+int mbert_attn_profile_enable(mbert_attn *h, int enable);
+
+/* Synchronise on the recorded events and return, per layer kind
+ * (index MBERT_GLOBAL / MBERT_LOCAL of the host arrays attn_ms[2] and
+ * attn_launches[2]), the summed attention-kernel milliseconds and the number
+ * of recorded kernels, plus the number of kernels enqueued by every entry
+ * point (*total_launches).  Clears all three.  Any output pointer may be
+ * NULL. */
+int mbert_attn_profile_read(mbert_attn *h, double *attn_ms, int64_t *attn_launches,
+                            int64_t *total_launches);
+
+/* Release the handle's device memory.  NULL is allowed.  The caller must
+ * make sure no enqueued work still uses the handle. */
+void mbert_attn_destroy(mbert_attn *h);
+
+/* Static, human-readable text for a status code. */
+const char *mbert_attn_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MBERT_ATTN_H */

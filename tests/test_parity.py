@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs.
+
+Tolerance (floating point): max |err| <= 2e-2 and mean |err| <= 2e-3 over
+every compared element, with the bf16 GPU output widened to fp64 and the
+oracle left unrounded.  Integer work (admitted-key counts of the tile
+schedule and mask) is compared bit-exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from encoder_only_transformer_gb300 import binding, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ERR = 2e-2
+MEAN_ERR = 2e-3
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    h = binding.Attention(0)
+    yield h
+    assert h.get_error() == 0
+    h.close()
+
+
+def _run(attn, wl, kind):
+    qkv = wl.qkv.cuda()
+    cu = wl.cu_seqlens.cuda()
+    out = attn.forward(qkv, cu, kind)
+    torch.cuda.synchronize()
+    assert attn.get_error() == 0
+    return out.cpu()
+
+
+def _compare(got_bf16, ref, what):
+    got = got_bf16.double().numpy()
+    assert got.shape == ref.shape
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    assert err.max() <= MAX_ERR and err.mean() <= MEAN_ERR, \
+        f"{what}: max|err| {err.max():.3e} mean|err| {err.mean():.3e}"
+    return err
+
+
+def _full_check(attn, wl, kind):
+    out = _run(attn, wl, kind)
+    ref, counts = oracle.attention_kind(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), kind)
+    _compare(out, ref, f"{wl.name} {kind}")
+    gc = attn.key_counts(wl.cu_seqlens.cuda(), wl.T, kind).cpu().numpy()
+    np.testing.assert_array_equal(gc, counts)
+    return out
+
+
+def _sampled_check(attn, wl, kind, per_seq, seed):
+    out = _run(attn, wl, kind)
+    rows = W.sample_rows(wl.cu_seqlens, per_seq, seed)
+    ref, counts = oracle.attention_kind(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), kind, rows=rows)
+    _compare(out[torch.from_numpy(rows)], ref, f"{wl.name} {kind} sampled")
+    gc = attn.key_counts(wl.cu_seqlens.cuda(), wl.T, kind).cpu().numpy()
+    np.testing.assert_array_equal(gc, oracle.key_counts(wl.cu_seqlens.numpy(),
+                                                        oracle.KINDS[kind]["half_window"]))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# small workloads: every row against the oracle
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [1, 2])
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_small_configs_full(attn, cfg, kind):
+    _full_check(attn, W.config(cfg), kind)
+
+
+EDGE_PACKS = {
+    "len1": [1],
+    "tile_edges": [127, 128, 129],
+    "two_tiles_ragged": [255, 256, 257],
+    "window_edges": [64, 65, 66, 193, 194],
+    "empties": [0, 5, 0, 300, 0],
+    "long_ragged": [1000, 3, 777],
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE_PACKS))
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_edge_packs(attn, name, kind):
+    _full_check(attn, W.custom(EDGE_PACKS[name], seed=len(name) * 7 + 3), kind)
+
+
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_many_tiny_sequences(attn, kind):
+    g = torch.Generator().manual_seed(77)
+    lengths = torch.randint(1, 21, (300,), generator=g).tolist()
+    _full_check(attn, W.custom(lengths, seed=78), kind)
+
+
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_length_one_returns_value_exactly(attn, kind):
+    wl = W.custom([1, 1, 3, 1], seed=5)
+    out = _run(attn, wl, kind)
+    v = wl.qkv[:, 1536:]
+    for r in (0, 1, 5):
+        assert torch.equal(out[r], v[r])
+
+
+# ---------------------------------------------------------------------------
+# the full-size workloads (sampled rows where the oracle would take long)
+# ---------------------------------------------------------------------------
+
+def test_config3_local_full(attn):
+    _full_check(attn, W.config(3), "local")
+
+
+def test_config3_global_sampled(attn):
+    _sampled_check(attn, W.config(3), "global", per_seq=384, seed=31)
+
+
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_config4_sampled(attn, kind):
+    _sampled_check(attn, W.config(4), kind, per_seq=24, seed=41)
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_config5_layer_sampled(attn, layer):
+    wl = W.config(5, layer=layer)
+    _sampled_check(attn, wl, W.layer_kind(layer), per_seq=8, seed=50 + layer)
+
+
+# ---------------------------------------------------------------------------
+# properties that hold at any size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_pad_sequence_leaves_real_rows_unchanged(attn, kind):
+    """A padded token packed as its own sequence does not change the real
+    outputs (gap 0, bit for bit)."""
+    real = W.custom([300, 41], seed=9)
+    padded = W.custom([300, 41, 5], seed=9)
+    a = _run(attn, real, kind)
+    b = _run(attn, padded, kind)
+    assert torch.equal(a, b[:341])
+
+
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_offset_in_pack_does_not_matter(attn, kind):
+    a = W.custom([333], seed=91)
+    b = W.custom([150], seed=92)
+    pack = W.Workload("pack", 0, 1.0, [150, 333], [kind], torch.cat([b.qkv, a.qkv]),
+                      W.cu_from_lengths([150, 333]))
+    alone = _run(attn, a, kind)
+    packed = _run(attn, pack, kind)
+    assert torch.equal(alone, packed[150:])
+
+
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_deterministic(attn, kind):
+    wl = W.config(2)
+    assert torch.equal(_run(attn, wl, kind), _run(attn, wl, kind))
+
+
+def test_global_equals_wide_band(attn):
+    """A handle whose band covers every sequence gives the global result on
+    its local layers when both use the same base."""
+    wide = binding.Attention(0, half_window=128, theta_local=160000.0)
+    try:
+        wl = W.custom([100, 129, 7], seed=13)   # every |i - j| <= 128
+        g = _run(attn, wl, "global")
+        qkv, cu = wl.qkv.cuda(), wl.cu_seqlens.cuda()
+        w = wide.forward(qkv, cu, "local").cpu()
+        assert wide.get_error() == 0
+        assert torch.equal(g, w)
+    finally:
+        wide.close()
+
+
+def test_no_write_outside_output(attn):
+    """Every output row is written and nothing past the end of out is."""
+    wl = W.custom([200, 1, 300], seed=17)
+    qkv, cu = wl.qkv.cuda(), wl.cu_seqlens.cuda()
+    buf = torch.full((wl.T + 64, 768), float("nan"), dtype=torch.bfloat16, device="cuda")
+    for kind in ("global", "local"):
+        buf.fill_(float("nan"))
+        attn.forward(qkv, cu, kind, out=buf[:wl.T])
+        torch.cuda.synchronize()
+        assert torch.isfinite(buf[:wl.T].float()).all()
+        assert torch.isnan(buf[wl.T:].float()).all()
+
+
+def test_runs_on_a_side_stream(attn):
+    wl = W.config(1)
+    qkv, cu = wl.qkv.cuda(), wl.cu_seqlens.cuda()
+    ref = attn.forward(qkv, cu, "global").cpu()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = attn.forward(qkv, cu, "global")
+    s.synchronize()
+    assert torch.equal(out.cpu(), ref)
+
+
+def test_module_level_function(attn):
+    wl = W.config(1)
+    out = binding.attention(wl.qkv.cuda(), wl.cu_seqlens.cuda(), "local")
+    torch.cuda.synchronize()
+    ref, _ = oracle.attention_kind(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), "local")
+    _compare(out.cpu(), ref, "module attention")
