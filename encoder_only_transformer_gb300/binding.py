@@ -39,6 +39,8 @@ SIGNATURES = {
     "mbert_attn_key_counts": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp]),
     "mbert_attn_get_error": (_c_int, [_vp]),
     "mbert_attn_selftest_timeout": (_c_int, [_vp, _c_i64, _vp]),
+    "mbert_attn_forward_noalloc": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp,
+                                            _vp]),
     "mbert_attn_profile_enable": (_c_int, [_vp, _c_int]),
     "mbert_attn_profile_read": (_c_int, [_vp, ctypes.POINTER(ctypes.c_double),
                                          ctypes.POINTER(ctypes.c_int64),

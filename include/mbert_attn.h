@@ -132,6 +132,36 @@ int mbert_attn_get_error(mbert_attn *h);
  * Nothing faults or traps; the context stays usable. */
 int mbert_attn_selftest_timeout(mbert_attn *h, int64_t limit_us, void *stream);
 
+/* Largest batch the allocation-free entry point below accepts: total
+ * tokens, and also sequences, per call. */
+#define MBERT_NOALLOC_MAX_TOKENS 8192
+
+/* The attention block without any device allocation.  The pages have no
+ * counterpart: this exists for callers that cannot call cudaMalloc -- a
+ * plugin inside a framework that owns all device memory through its own
+ * pool, a service whose memory is reserved once at start-up, or a loop that
+ * cannot take the device-wide synchronisation cudaMalloc/cudaFree may
+ * cause.  Such callers cannot create a handle, so this call needs none.
+ *   Arguments as for mbert_attn_forward, on the current CUDA device, with
+ *   the ModernBERT-base defaults (half window 64, bases 160000 / 10000).
+ *   device_status  device int32 or NULL: receives the device-side error bits
+ *                  of this call (0 = ok, 1 = bad cu_seqlens, 2 = a sequence
+ *                  longer than max_seqlen, 4 = a bounded wait timed out),
+ *                  written on `stream` after the kernels.
+ * Scratch memory (work list, rotated Q/K rows, RoPE tables: about 28 MiB)
+ * is one static device array that every GPU that loads this part of the
+ * library holds until the process exits.  total_tokens or n_seqs above
+ * MBERT_NOALLOC_MAX_TOKENS, or max_seqlen above it, are rejected
+ * (MBERT_ERR_BAD_ARG / MBERT_ERR_SEQ_TOO_LONG) before anything is enqueued.
+ * The first call on a device does a one-time set-up (it looks up the
+ * array's device address and fills the RoPE tables with synchronous
+ * copies); make that first call before any stream capture.  Every call
+ * shares the array and overwrites what the previous call left there, so two
+ * calls whose work overlaps on the GPU (e.g. on different streams) race. */
+int mbert_attn_forward_noalloc(const void *qkv, const int32_t *cu_seqlens, int n_seqs,
+                               int64_t total_tokens, int max_seqlen, int layer_kind,
+                               void *out, int32_t *device_status, void *stream);
+
 /* Measurement.  While enabled, every mbert_attn_forward also records a
  * CUDA event pair on its stream around its attention kernel (the plan and
  * RoPE kernels before it are outside the pair).  The handle always counts
