@@ -127,6 +127,7 @@ attn_generic_kernel(const __grid_constant__ CUtensorMap tm_rot,
         }
         if (!(ok = mbar_wait(bar_s, t & 1, err)))
             break;
+        __syncwarp();
         tc_fence_after();
 
         float s[kBlockN];

@@ -331,6 +331,11 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
     if (rc != MBERT_OK)
         return rc;
     Plan p = make_plan(h, cu_seqlens, n_seqs, T, max_seqlen);
+    if (layer_kind == MBERT_GLOBAL) {
+        // the global kernel takes 256 query rows (two 128-row tiles) per entry
+        p.block = 2 * kBlockM;
+        p.entry_bound = static_cast<int>((T + (p.block - 1) * static_cast<int64_t>(n_seqs)) / p.block);
+    }
 
     AttnArgs a;
     if (encode_map(h, &a.tm_rot, h->rot, 2 * kHidden, T) != MBERT_OK ||
@@ -364,7 +369,7 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
     if (e == cudaSuccess && ev0)
         e = cudaEventRecord(ev0, st);
     if (e == cudaSuccess)
-        e = launch_attn_generic(a, st);
+        e = layer_kind == MBERT_GLOBAL ? launch_attn_global(a, st) : launch_attn_generic(a, st);
     if (e == cudaSuccess && ev1)
         e = cudaEventRecord(ev1, st);
     h->launches += 3;

@@ -12,6 +12,7 @@ namespace mbert {
 // Work list written by the plan kernel: one entry per (sequence, 128-query
 // block), longest sequences first; the attention grid covers entries x heads.
 struct Plan {
+    int block = 128;        // query rows per work entry (128 or 256)
     const int32_t *cu;      // device [n_seqs + 1]
     int n_seqs;
     int64_t T;
@@ -49,7 +50,12 @@ struct AttnArgs {
 cudaError_t launch_wait_timeout_selftest(int32_t *err, unsigned long long limit_ns,
                                          cudaStream_t stream);
 
-// Generic flash attention over pre-rotated Q/K: one CTA per (entry, head).
+// Generic flash attention over pre-rotated Q/K: one CTA per (entry, head),
+// entries of 128 query rows.
 cudaError_t launch_attn_generic(const AttnArgs &a, cudaStream_t stream);
+
+// Global-layer attention over pre-rotated Q/K: one CTA per (entry, head),
+// entries of 256 query rows, warp-specialised tcgen05 pipeline.
+cudaError_t launch_attn_global(const AttnArgs &a, cudaStream_t stream);
 
 }  // namespace mbert

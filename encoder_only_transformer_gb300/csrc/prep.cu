@@ -41,11 +41,11 @@ __device__ int block_inclusive_scan(int v, int *warp_sums)
 
 // One block.  Checks cu_seqlens (cu[0] == 0, non-decreasing, cu[n] == T,
 // every length <= max_seqlen) and writes the work list: for each sequence,
-// its ceil(L/128) query blocks, sequences ordered by decreasing block count
+// its ceil(L/blk) query blocks of blk rows, sequences ordered by decreasing block count
 // (longest-processing-time first; the order inside a bin is arbitrary and
 // does not affect any result).
 __global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seqlen,
+plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seqlen, int blk,
             int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count)
 {
     __shared__ int s_bad;
@@ -53,7 +53,7 @@ plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seq
     __shared__ int s_off[kMaxBins + 1];
     __shared__ int s_warp[32];
     const int tid = threadIdx.x;
-    const int nbmax = (max_seqlen + kBlockM - 1) / kBlockM;   // <= kMaxBins (host-checked)
+    const int nbmax = (max_seqlen + blk - 1) / blk;   // <= kMaxBins (host-checked)
 
     if (tid == 0)
         s_bad = 0;
@@ -69,7 +69,7 @@ plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seq
         else if (L > max_seqlen)
             atomicOr(&s_bad, kErrTooLong);
         else
-            atomicAdd(&s_hist[(L + kBlockM - 1) / kBlockM], 1);
+            atomicAdd(&s_hist[(L + blk - 1) / blk], 1);
     }
     __syncthreads();
     if (s_bad) {
@@ -96,7 +96,7 @@ plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seq
     __syncthreads();
     for (int s = tid; s < n_seqs; s += kPlanThreads) {
         const int L = cu[s + 1] - cu[s];
-        const int nb = (L + kBlockM - 1) / kBlockM;
+        const int nb = (L + blk - 1) / blk;
         if (nb == 0)
             continue;
         const int slot = atomicAdd(&s_hist[nb], 1);
@@ -225,8 +225,8 @@ cudaError_t launch_wait_timeout_selftest(int32_t *err, unsigned long long limit_
 
 cudaError_t launch_plan(const Plan &p, cudaStream_t stream)
 {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(p.cu, p.n_seqs, p.T, p.max_seqlen, p.err,
-                                                  p.work, p.work_count);
+    plan_kernel<<<1, kPlanThreads, 0, stream>>>(p.cu, p.n_seqs, p.T, p.max_seqlen, p.block,
+                                                  p.err, p.work, p.work_count);
     return cudaGetLastError();
 }
 
