@@ -1,58 +1,74 @@
-// Global-layer attention over pre-rotated Q/K: a warp-specialised tcgen05
-// pipeline for sm_103a.
+// Global-layer attention over pre-rotated Q/K: a persistent, warp-specialised
+// tcgen05 pipeline for sm_103a.
 //
-// One CTA (12 warps) per (work entry, head); an entry is 256 query rows of
-// one sequence, split into two 128-row tiles that share every K/V tile:
-//   warps 0-3  softmax group 0 (query tile 0, TMEM lanes 0..127)
-//   warps 4-7  softmax group 1 (query tile 1)
-//   warp  8    TMA producer: Q0, Q1 once, then K and V through 3-stage rings
-//   warp  9    MMA issuer (the whole warp runs the loop; one elected lane
-//              issues): S_w = Q_w K_j^T and O_w += P_w V_j
-//   warps 10-11 idle (they complete the third warpgroup, whose registers
-//              go to the softmax groups)
+// Work: a unit is (work entry, head), an entry being 256 query rows of one
+// sequence; a unit needs ceil(L/128) key tiles.  All (unit, key tile)
+// iterations, in work-list order, are split into equal contiguous ranges, one
+// per persistent CTA (one CTA per SM), so every SM gets the same number of
+// tile iterations whatever the number of units.  A CTA walks its range as a
+// sequence of segments (a unit and a run of its key tiles).  A segment that
+// covers its whole unit writes the output directly; a unit cut between CTAs
+// leaves one partial state (unnormalised O, row maximum, row sum) per
+// segment in a workspace, and whichever CTA completes the unit's last
+// segment (an atomic counter per unit decides) merges them, always in CTA
+// order, so results are reproducible run to run.  No CTA ever waits for
+// another.  (Where a unit is cut depends on the whole batch, so adding a
+// sequence to a pack can change another sequence's outputs by rounding.)
+//
+// CTA (12 warps):
+//   warps 0-3   softmax group 0 (query tile 0 of the entry, TMEM lanes 0..127)
+//   warps 4-7   softmax group 1 (query tile 1)
+//   warp  8     TMA producer: Q tiles (double-buffered per segment), K and V
+//               through 3-stage rings
+//   warps 9,10  MMA issuers, one per query tile (whole warp runs the loop;
+//               one elected lane issues): S_w = Q_w K^T, O_w += P_w V
+//   warp  11    idle (completes the third warpgroup, whose registers go to the
+//               softmax groups)
 // TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384)
-// O0 [384,448) O1 [448,512), all fp32 except P (bf16 pairs).  The issue
-// order S0(j+1), S1(j+1), PV0(j), PV1(j) keeps the tensor core fed while
-// each softmax group works on its previous tile.
+// O0 [384,448) O1 [448,512); fp32 except P (bf16 pairs).
 //
 // Arithmetic ("ModernBERT-base Architecture Teardown", "How Does
 // Self-Attention Work?"): scores q.k / 8, softmax over every key of the
 // sequence (a global layer, "What Are Local and Global Attention?"), output
-// the weighted blend of V.  The softmax is online in base 2; the running
-// maximum is only raised (and O rescaled) when a tile's maximum exceeds it
-// by more than 8, so the unnormalised weights stay below 2^8 and O and the
-// row sum always use the same reference.
+// the weighted blend of V.  The softmax is online in base 2; the reference
+// maximum only moves (and O is rescaled) when a tile's maximum exceeds it by
+// more than 8, so O and the row sum always share one reference.  Partial
+// states over disjoint key ranges are merged exactly:
+// m = max(m_a, m_b), O = O_a 2^(m_a - m) + O_b 2^(m_b - m), likewise l.
 #include "common.cuh"
 #include "internal.h"
 
 namespace mbert {
 namespace {
 
-constexpr int kThreads = 384;      // 3 warpgroups
-// Registers per thread after the split: the producer/MMA warpgroup gives up
-// registers to the two softmax warpgroups (4 x 88 + 8 x 208 = 12 x 168, the
-// launch budget).
-constexpr int kRegsSoftmax = 208;
+constexpr int kThreads = 384;
+constexpr int kRegsSoftmax = 208;   // 4 x 88 + 8 x 208 = 12 x 168 (the launch budget)
 constexpr int kRegsControl = 88;
 constexpr int kStages = 3;
-constexpr uint32_t kOffQ = 0;                                  // Q0, Q1
-constexpr uint32_t kOffK = 2 * kTileBytes;                     // K ring
+
+constexpr uint32_t kOffQ = 0;                                  // 2 sets of (Q0, Q1)
+constexpr uint32_t kOffK = 4 * kTileBytes;                     // K ring
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;       // V ring
-constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;     // 131072
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;     // 163840
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 
 // barrier slots (8 bytes each) from kOffBar
-constexpr int kBarQ = 0;
-constexpr int kBarKFull = 1;      // + stage
-constexpr int kBarKEmpty = 4;     // + stage
-constexpr int kBarVFull = 7;      // + stage
-constexpr int kBarVEmpty = 10;    // + stage
-constexpr int kBarSFull = 13;     // + group
-constexpr int kBarSEmpty = 15;    // + group
-constexpr int kBarPFull = 17;     // + group
-constexpr int kBarODone = 19;     // + group
-constexpr int kNumBars = 21;
-constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;
+constexpr int kBarQFull = 0;      // + set (2)
+constexpr int kBarQEmpty = 2;     // + set
+constexpr int kBarKFull = 4;      // + stage (3)
+constexpr int kBarKEmpty = 7;
+constexpr int kBarVFull = 10;
+constexpr int kBarVEmpty = 13;
+constexpr int kBarSFull = 16;     // + group (2)
+constexpr int kBarSEmpty = 18;
+constexpr int kBarPFull = 20;
+constexpr int kBarODone = 22;
+constexpr int kBarOFree = 24;
+constexpr int kBarSegSync = 26;   // all 256 softmax threads wrote their partial rows
+constexpr int kBarSegFlag = 27;   // the counter result is in shared memory
+constexpr int kNumBars = 28;
+constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;          // TMEM address
+constexpr uint32_t kOffFlag = kOffSlot + 8;                    // "I merge" flag
 
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int w) { return 128u * w; }
@@ -91,58 +107,148 @@ __device__ __forceinline__ void fadd2(float &a0, float &a1, float b0, float b1)
     asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(d));
 }
 
+// ---------------------------------------------------------------- schedule
+struct Params {
+    const int32_t *cu;
+    const int2 *work;
+    const int32_t *tile_start;   // [entries + 1]
+    int32_t *unit_cnt;
+    float *partials;
+    __nv_bfloat16 *out;
+    int32_t *err;
+    int entries;
+    long long total;             // iterations of all units
+    int ctas;
+};
+
+__device__ __forceinline__ long long range_lo(const Params &p, int c)
+{
+    return static_cast<long long>(c) * p.total / p.ctas;
+}
+
+// The CTA whose range contains iteration `it`.
+__device__ __forceinline__ int cta_of(const Params &p, long long it)
+{
+    int c = static_cast<int>((it * p.ctas) / p.total);
+    while (c + 1 < p.ctas && range_lo(p, c + 1) <= it)
+        ++c;
+    while (c > 0 && range_lo(p, c) > it)
+        --c;
+    return c;
+}
+
+// A run of key tiles [kb, ke) of one unit.
+struct Seg {
+    int entry, head, kb, ke, ntiles;
+    int row0, L, q0;
+    long long ua;              // first iteration of the unit
+};
+
+// Walks the segments of one CTA's range [it, hi).
+struct SegIter {
+    long long it, hi;
+    int entry;
+
+    __device__ void init(const Params &p, int c)
+    {
+        it = range_lo(p, c);
+        hi = range_lo(p, c + 1);
+        int lo = 0, h = p.entries;           // entry with tile_start <= it
+        while (h - lo > 1) {
+            const int mid = (lo + h) >> 1;
+            if (p.tile_start[mid] <= it)
+                lo = mid;
+            else
+                h = mid;
+        }
+        entry = lo;
+    }
+
+    __device__ bool next(const Params &p, Seg &s)
+    {
+        if (it >= hi)
+            return false;
+        while (entry + 1 < p.entries && p.tile_start[entry + 1] <= it)
+            ++entry;
+        const int2 w = p.work[entry];
+        s.entry = entry;
+        s.row0 = p.cu[w.x];
+        s.L = p.cu[w.x + 1] - s.row0;
+        s.q0 = w.y * 2 * kBlockM;
+        s.ntiles = (s.L + kBlockN - 1) / kBlockN;
+        const long long off = it - p.tile_start[entry];
+        s.head = static_cast<int>(off / s.ntiles);
+        s.kb = static_cast<int>(off % s.ntiles);
+        const long long left = hi - it;
+        s.ke = static_cast<int>(left < s.ntiles - s.kb ? s.kb + left : s.ntiles);
+        s.ua = p.tile_start[entry] + static_cast<long long>(s.head) * s.ntiles;
+        it += s.ke - s.kb;
+        return true;
+    }
+};
+
 struct Ctx {
     uint32_t base;          // 1024-aligned shared address
     uint32_t tmem;
-    int row0, L, q0, head, ntiles;
+    uint8_t *sbase;         // generic pointer to the same address
 };
 
 __device__ __forceinline__ uint32_t bar(const Ctx &c, int i) { return c.base + kOffBar + 8u * i; }
 
 // ---------------------------------------------------------------- producer
-__device__ void producer(const Ctx &c, const CUtensorMap *tm_rot, const CUtensorMap *tm_qkv,
-                         int *err)
+__device__ void producer(const Ctx &c, const Params &p, const CUtensorMap *tm_rot,
+                         const CUtensorMap *tm_qkv, int cta)
 {
     const uint64_t keep = l2_policy_evict_last();    // K/V: re-read by every query block
     const uint64_t once = l2_policy_evict_first();   // Q: read once
-    const int colQ = c.head * kHeadDim;
-    const int colK = kHidden + c.head * kHeadDim;
-    const int colV = 2 * kHidden + c.head * kHeadDim;
-    mbar_arrive_expect_tx(bar(c, kBarQ), 2 * kTileBytes);
-    tma_load_2d_hint(c.base + kOffQ, tm_rot, colQ, c.row0 + c.q0, bar(c, kBarQ), once);
-    tma_load_2d_hint(c.base + kOffQ + kTileBytes, tm_rot, colQ, c.row0 + c.q0 + kBlockM,
-                     bar(c, kBarQ), once);
-    for (int j = 0; j < c.ntiles; ++j) {
-        const int s = j % kStages;
-        const uint32_t u = j / kStages;
-        const int krow = c.row0 + j * kBlockN;
-        if (u > 0 && !mbar_wait(bar(c, kBarKEmpty + s), (u - 1) & 1, err))
+    SegIter si;
+    si.init(p, cta);
+    Seg s;
+    uint32_t g = 0;          // key tiles issued by this CTA so far
+    for (uint32_t sg = 0; si.next(p, s); ++sg) {
+        const int qs = sg & 1;
+        if (sg >= 2 && !mbar_wait(bar(c, kBarQEmpty + qs), ((sg >> 1) - 1) & 1, p.err))
             return;
-        mbar_arrive_expect_tx(bar(c, kBarKFull + s), kTileBytes);
-        tma_load_2d_hint(c.base + kOffK + s * kTileBytes, tm_rot, colK, krow, bar(c, kBarKFull + s), keep);
-        if (u > 0 && !mbar_wait(bar(c, kBarVEmpty + s), (u - 1) & 1, err))
-            return;
-        mbar_arrive_expect_tx(bar(c, kBarVFull + s), kTileBytes);
-        tma_load_2d_hint(c.base + kOffV + s * kTileBytes, tm_qkv, colV, krow, bar(c, kBarVFull + s), keep);
+        const int colQ = s.head * kHeadDim;
+        const int colK = kHidden + s.head * kHeadDim;
+        const int colV = 2 * kHidden + s.head * kHeadDim;
+        const uint32_t qdst = c.base + kOffQ + qs * 2 * kTileBytes;
+        mbar_arrive_expect_tx(bar(c, kBarQFull + qs), 2 * kTileBytes);
+        tma_load_2d_hint(qdst, tm_rot, colQ, s.row0 + s.q0, bar(c, kBarQFull + qs), once);
+        tma_load_2d_hint(qdst + kTileBytes, tm_rot, colQ, s.row0 + s.q0 + kBlockM,
+                         bar(c, kBarQFull + qs), once);
+        for (int k = s.kb; k < s.ke; ++k, ++g) {
+            const int st = g % kStages;
+            const uint32_t u = g / kStages;
+            const int krow = s.row0 + k * kBlockN;
+            if (u > 0 && !mbar_wait(bar(c, kBarKEmpty + st), (u - 1) & 1, p.err))
+                return;
+            mbar_arrive_expect_tx(bar(c, kBarKFull + st), kTileBytes);
+            tma_load_2d_hint(c.base + kOffK + st * kTileBytes, tm_rot, colK, krow,
+                             bar(c, kBarKFull + st), keep);
+            if (u > 0 && !mbar_wait(bar(c, kBarVEmpty + st), (u - 1) & 1, p.err))
+                return;
+            mbar_arrive_expect_tx(bar(c, kBarVFull + st), kTileBytes);
+            tma_load_2d_hint(c.base + kOffV + st * kTileBytes, tm_qkv, colV, krow,
+                             bar(c, kBarVFull + st), keep);
+        }
     }
 }
 
-// ---------------------------------------------------------------- MMA issuer
-// The MMA issuer runs on the whole (converged) warp 9: descriptors are
-// computed by every lane, and the *_warp wrappers let one elected lane issue.
-__device__ __forceinline__ void issue_s(const Ctx &c, int w, int s)
+// ---------------------------------------------------------------- MMA issuers
+__device__ __forceinline__ void issue_s(const Ctx &c, int w, int qs, int st)
 {
-    const uint32_t q = c.base + kOffQ + w * kTileBytes;
-    const uint32_t k = c.base + kOffK + s * kTileBytes;
+    const uint32_t q = c.base + kOffQ + (qs * 2 + w) * kTileBytes;
+    const uint32_t k = c.base + kOffK + st * kTileBytes;
 #pragma unroll
     for (int kk = 0; kk < kHeadDim / 16; ++kk)
         mma_bf16_ss_warp(c.tmem + col_s(w), make_sdesc_sw128(q + 32 * kk, 16, 1024),
                          make_sdesc_sw128(k + 32 * kk, 16, 1024), kIdescS, kk > 0);
 }
 
-__device__ __forceinline__ void issue_o(const Ctx &c, int w, int s, bool accumulate)
+__device__ __forceinline__ void issue_o(const Ctx &c, int w, int st, bool accumulate)
 {
-    const uint32_t v = c.base + kOffV + s * kTileBytes;
+    const uint32_t v = c.base + kOffV + st * kTileBytes;
 #pragma unroll
     for (int kk = 0; kk < kBlockN / 16; ++kk)
         mma_bf16_ts_warp(c.tmem + col_o(w), c.tmem + col_p(w) + 8 * kk,
@@ -150,184 +256,276 @@ __device__ __forceinline__ void issue_o(const Ctx &c, int w, int s, bool accumul
                          (accumulate || kk > 0) ? 1u : 0u);
 }
 
-__device__ void mma_issuer(const Ctx &c, int *err)
+// Issuer for query tile w: per segment, S_w(t) for each key tile t, and
+// O_w += P_w(t-1) V(t-1) one tile behind, so that S of the next tile is
+// computed while the softmax group works on the current one.
+__device__ void mma_issuer(const Ctx &c, const Params &p, int w, int cta)
 {
-    if (!mbar_wait(bar(c, kBarQ), 0, err) || !mbar_wait(bar(c, kBarKFull), 0, err))
-        return;
-    __syncwarp();
-    tc_fence_after();
-    issue_s(c, 0, 0);
-    mma_commit_warp(bar(c, kBarSFull + 0));
-    issue_s(c, 1, 0);
-    mma_commit_warp(bar(c, kBarSFull + 1));
-    mma_commit_warp(bar(c, kBarKEmpty + 0));
-    for (int j = 0; j < c.ntiles; ++j) {
-        const uint32_t ph = j & 1;
-        if (j + 1 < c.ntiles) {
-            const int s1 = (j + 1) % kStages;
-            const uint32_t u1 = (j + 1) / kStages;
-            if (!mbar_wait(bar(c, kBarKFull + s1), u1 & 1, err))
-                return;
-            if (!mbar_wait(bar(c, kBarSEmpty + 0), ph, err))
-                return;
-            __syncwarp();
-            tc_fence_after();
-            issue_s(c, 0, s1);
-            mma_commit_warp(bar(c, kBarSFull + 0));
-            if (!mbar_wait(bar(c, kBarSEmpty + 1), ph, err))
-                return;
-            __syncwarp();
-            tc_fence_after();
-            issue_s(c, 1, s1);
-            mma_commit_warp(bar(c, kBarSFull + 1));
-            mma_commit_warp(bar(c, kBarKEmpty + s1));
+    SegIter si;
+    si.init(p, cta);
+    Seg s;
+    uint32_t g0 = 0;
+    for (uint32_t sg = 0; si.next(p, s); ++sg) {
+        const int qs = sg & 1;
+        const int n = s.ke - s.kb;
+        if (!mbar_wait(bar(c, kBarQFull + qs), (sg >> 1) & 1, p.err))
+            return;
+        for (int t = 0; t <= n; ++t) {
+            if (t < n) {
+                const uint32_t g = g0 + t;
+                const int st = g % kStages;
+                if (!mbar_wait(bar(c, kBarKFull + st), (g / kStages) & 1, p.err))
+                    return;
+                if (g > 0 && !mbar_wait(bar(c, kBarSEmpty + w), (g - 1) & 1, p.err))
+                    return;
+                __syncwarp();
+                tc_fence_after();
+                issue_s(c, w, qs, st);
+                mma_commit_warp(bar(c, kBarSFull + w));
+                mma_commit_warp(bar(c, kBarKEmpty + st));
+                if (t == n - 1)
+                    mma_commit_warp(bar(c, kBarQEmpty + qs));
+            }
+            if (t > 0) {
+                const uint32_t g = g0 + t - 1;
+                const int st = g % kStages;
+                if (!mbar_wait(bar(c, kBarVFull + st), (g / kStages) & 1, p.err))
+                    return;
+                if (!mbar_wait(bar(c, kBarPFull + w), g & 1, p.err))
+                    return;
+                if (t == 1 && sg > 0 && !mbar_wait(bar(c, kBarOFree + w), (sg - 1) & 1, p.err))
+                    return;
+                __syncwarp();
+                tc_fence_after();
+                issue_o(c, w, st, t > 1);
+                mma_commit_warp(bar(c, kBarODone + w));
+                mma_commit_warp(bar(c, kBarVEmpty + st));
+            }
         }
-        const int s = j % kStages;
-        const uint32_t u = j / kStages;
-        if (!mbar_wait(bar(c, kBarVFull + s), u & 1, err))
-            return;
-        if (!mbar_wait(bar(c, kBarPFull + 0), ph, err))
-            return;
-        __syncwarp();
-        tc_fence_after();
-        issue_o(c, 0, s, j > 0);
-        mma_commit_warp(bar(c, kBarODone + 0));
-        if (!mbar_wait(bar(c, kBarPFull + 1), ph, err))
-            return;
-        __syncwarp();
-        tc_fence_after();
-        issue_o(c, 1, s, j > 0);
-        mma_commit_warp(bar(c, kBarODone + 1));
-        mma_commit_warp(bar(c, kBarVEmpty + s));
+        g0 += n;
     }
 }
 
 // ---------------------------------------------------------------- softmax
-__device__ void softmax_group(const Ctx &c, int w, int warp_in_group, int lane,
-                              __nv_bfloat16 *__restrict__ out, int *err)
+__device__ __forceinline__ float *partial_slot(const Params &p, int slot)
+{
+    return p.partials + static_cast<size_t>(slot) * kPartialFloats;
+}
+
+// Slot used by CTA cc for the unit starting at iteration ua: its first slot
+// when the unit is (or starts) its first segment, else its second.
+__device__ __forceinline__ int slot_of(const Params &p, int cc, long long ua)
+{
+    return range_lo(p, cc) >= ua ? 2 * cc : 2 * cc + 1;
+}
+
+__device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_group,
+                              int lane, int cta)
 {
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp_in_group) << 16;
     const uint32_t tS = c.tmem + col_s(w) + lane_off;
     const uint32_t tP = c.tmem + col_p(w) + lane_off;
     const uint32_t tO = c.tmem + col_o(w) + lane_off;
-    const int qpos = c.q0 + kBlockM * w + 32 * warp_in_group + lane;
-    float m = -INFINITY;    // running reference maximum (scaled, base 2)
-    float l = 0.f;          // running sum of exp2(score - m)
-    bool ok = true;
+    const int r = 32 * warp_in_group + lane;          // row within the query tile
+    const int rr = kBlockM * w + r;                   // row within the entry
+    volatile int *flag = reinterpret_cast<volatile int *>(c.sbase + kOffFlag);
+    SegIter si;
+    si.init(p, cta);
+    Seg s;
+    uint32_t g0 = 0, npartial = 0;
+    for (uint32_t sg = 0; si.next(p, s); ++sg) {
+        const int n = s.ke - s.kb;
+        float m = -INFINITY;    // running reference maximum (scaled, base 2)
+        float l = 0.f;          // running sum of exp2(score - m)
+        for (int t = 0; t < n; ++t) {
+            const uint32_t g = g0 + t;
+            if (!mbar_wait(bar(c, kBarSFull + w), g & 1, p.err))
+                return;
+            __syncwarp();
+            tc_fence_after();
+            float sc[kBlockN];
+            {
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tmem_ld32(tS, r0);
+                tmem_ld32(tS + 32, r1);
+                tmem_ld32(tS + 64, r2);
+                tmem_ld32(tS + 96, r3);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    sc[i] = __uint_as_float(r0[i]);
+                    sc[32 + i] = __uint_as_float(r1[i]);
+                    sc[64 + i] = __uint_as_float(r2[i]);
+                    sc[96 + i] = __uint_as_float(r3[i]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(c, kBarSEmpty + w));   // S may be overwritten now
 
-    for (int j = 0; j < c.ntiles; ++j) {
-        if (!(ok = mbar_wait(bar(c, kBarSFull + w), j & 1, err)))
-            break;
+            const int kvalid = s.L - (s.kb + t) * kBlockN;   // keys of this tile in the sequence
+            if (kvalid < kBlockN) {
+#pragma unroll
+                for (int i = 0; i < kBlockN; ++i)
+                    if (i >= kvalid)
+                        sc[i] = -INFINITY;
+            }
+            // row maximum: 8 independent chains of 3-input max, then combine
+            float mp[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mp[k] = fmax3(sc[k], sc[8 + k], sc[16 + k]);
+#pragma unroll
+            for (int i = 24; i < kBlockN; i += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mp[k] = fmax3(mp[k], sc[i + k], sc[i + 8 + k]);
+            const float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]),
+                                   fmaxf(fmax3(mp[3], mp[4], mp[5]), fmax3(mp[6], mp[7], mp[7])));
+            const float mc = mx * kScaleLog2;
+            const bool need = mc > m + kRescaleThreshold;
+            const float mn = need ? mc : m;
+            const float alpha = need ? ex2_approx(m - mn) : 1.f;
+            const float neg = -mn;
+
+            // p = 2^(s * scale - m), packed to bf16 pairs; row sum in 4
+            // independent fp32x2 accumulators
+            uint32_t pk[kBlockN / 2];
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < kBlockN / 2; ++i) {
+                float x0 = sc[2 * i], x1 = sc[2 * i + 1];
+                ffma2_bc(x0, x1, kScaleLog2, neg);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                const int a = 2 * (i & 3);
+                fadd2(acc[a], acc[a + 1], p0, p1);
+                pk[i] = pack_bf16x2(p0, p1);
+            }
+            fadd2(acc[0], acc[1], acc[2], acc[3]);
+            fadd2(acc[4], acc[5], acc[6], acc[7]);
+            fadd2(acc[0], acc[1], acc[4], acc[5]);
+
+            if (t > 0) {
+                // P_w and O_w are free once the previous P V has completed
+                if (!mbar_wait(bar(c, kBarODone + w), (g - 1) & 1, p.err))
+                    return;
+                __syncwarp();
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32 * h, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + 32 * h, o);
+                    }
+                }
+            }
+            l = l * alpha + (acc[0] + acc[1]);
+            m = mn;
+            tmem_st64(tP, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(c, kBarPFull + w));
+        }
+        g0 += n;
+
+        // ---- end of the segment: O of this segment in registers
+        if (!mbar_wait(bar(c, kBarODone + w), (g0 - 1) & 1, p.err))
+            return;
         __syncwarp();
         tc_fence_after();
-        float s[kBlockN];
+        float o[kHeadDim];
         {
-            uint32_t r0[32], r1[32], r2[32], r3[32];
-            tmem_ld32(tS, r0);
-            tmem_ld32(tS + 32, r1);
-            tmem_ld32(tS + 64, r2);
-            tmem_ld32(tS + 96, r3);
+            uint32_t a[32], b[32];
+            tmem_ld32(tO, a);
+            tmem_ld32(tO + 32, b);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                s[i] = __uint_as_float(r0[i]);
-                s[32 + i] = __uint_as_float(r1[i]);
-                s[64 + i] = __uint_as_float(r2[i]);
-                s[96 + i] = __uint_as_float(r3[i]);
+                o[i] = __uint_as_float(a[i]);
+                o[32 + i] = __uint_as_float(b[i]);
             }
         }
         tc_fence_before();
-        mbar_arrive(bar(c, kBarSEmpty + w));   // S may be overwritten now
+        mbar_arrive(bar(c, kBarOFree + w));   // the next segment may reset O
 
-        const int kvalid = c.L - j * kBlockN;   // keys of this tile inside the sequence
-        if (kvalid < kBlockN) {
+        bool write = true;
+        if (n != s.ntiles) {
+            // The unit is split between CTAs: leave this segment's state in
+            // the workspace, and merge if this is the unit's last segment.
+            const long long ua = s.ua, ub = s.ua + s.ntiles;
+            float *mine = partial_slot(p, slot_of(p, cta, ua));
+            float4 *dst = reinterpret_cast<float4 *>(mine + rr * kHeadDim);
 #pragma unroll
-            for (int i = 0; i < kBlockN; ++i)
-                if (i >= kvalid)
-                    s[i] = -INFINITY;
-        }
-        // row maximum: 8 independent chains of 3-input max, then combine
-        float mp[8];
+            for (int i = 0; i < kHeadDim / 4; ++i)
+                dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            reinterpret_cast<float2 *>(mine + kPartialRows * kHeadDim)[rr] = make_float2(m, l);
+            __threadfence();
+            mbar_arrive(bar(c, kBarSegSync));
+            if (w == 0 && r == 0) {
+                int last = 0;
+                if (mbar_wait(bar(c, kBarSegSync), npartial & 1, p.err)) {
+                    const int c_first = cta_of(p, ua), c_last = cta_of(p, ub - 1);
+                    const int nseg = c_last - c_first + 1;
+                    const int unit = s.entry * kHeads + s.head;
+                    last = atomicAdd(p.unit_cnt + unit, 1) == nseg - 1;
+                    __threadfence();
+                }
+                *flag = last;
+                mbar_arrive(bar(c, kBarSegFlag));
+            }
+            if (!mbar_wait(bar(c, kBarSegFlag), npartial & 1, p.err))
+                return;
+            ++npartial;
+            write = *flag != 0;
+            if (write) {
+                // Merge every segment's state (this CTA's included) in CTA
+                // order, so that the result does not depend on which CTA
+                // finished last.
+                const int c_first = cta_of(p, ua), c_last = cta_of(p, ub - 1);
+                m = -INFINITY;
+                l = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            mp[k] = fmax3(s[k], s[8 + k], s[16 + k]);
+                for (int i = 0; i < kHeadDim; ++i)
+                    o[i] = 0.f;
+                for (int cc = c_first; cc <= c_last; ++cc) {
+                    const float *part = partial_slot(p, slot_of(p, cc, ua));
+                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(part + kPartialRows * kHeadDim) + rr);
+                    const float mnew = fmaxf(m, ml.x);
+                    const float a = cc == c_first ? 0.f : ex2_approx(m - mnew);
+                    const float b = ex2_approx(ml.x - mnew);
+                    const float4 *src = reinterpret_cast<const float4 *>(part + rr * kHeadDim);
 #pragma unroll
-        for (int i = 24; i < kBlockN; i += 16)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mp[k] = fmax3(mp[k], s[i + k], s[i + 8 + k]);
-        const float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]),
-                               fmaxf(fmax3(mp[3], mp[4], mp[5]), fmax3(mp[6], mp[7], mp[7])));
-        const float mc = mx * kScaleLog2;
-        const bool need = mc > m + kRescaleThreshold;
-        const float mn = need ? mc : m;
-        const float alpha = need ? ex2_approx(m - mn) : 1.f;
-        const float neg = -mn;
-
-        // p = 2^(s * scale - m), packed to bf16 pairs; row sum in 4
-        // independent fp32x2 accumulators
-        uint32_t pk[kBlockN / 2];
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < kBlockN / 2; ++i) {
-            float x0 = s[2 * i], x1 = s[2 * i + 1];
-            ffma2_bc(x0, x1, kScaleLog2, neg);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            const int a = 2 * (i & 3);
-            fadd2(acc[a], acc[a + 1], p0, p1);
-            pk[i] = pack_bf16x2(p0, p1);
-        }
-        fadd2(acc[0], acc[1], acc[2], acc[3]);
-        fadd2(acc[4], acc[5], acc[6], acc[7]);
-        fadd2(acc[0], acc[1], acc[4], acc[5]);
-        const float a0 = acc[0], a1 = acc[1];
-
-        if (j > 0) {
-            // P_w and O_w are free once the previous P V has completed
-            if (!(ok = mbar_wait(bar(c, kBarODone + w), (j - 1) & 1, err)))
-                break;
-            __syncwarp();
-            tc_fence_after();
-            if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + 32 * h, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tO + 32 * h, o);
+                    for (int i = 0; i < kHeadDim / 4; ++i) {
+                        const float4 v = __ldcg(src + i);
+                        o[4 * i] = o[4 * i] * a + v.x * b;
+                        o[4 * i + 1] = o[4 * i + 1] * a + v.y * b;
+                        o[4 * i + 2] = o[4 * i + 2] * a + v.z * b;
+                        o[4 * i + 3] = o[4 * i + 3] * a + v.w * b;
+                    }
+                    l = l * a + ml.y * b;
+                    m = mnew;
                 }
             }
         }
-        l = l * alpha + (a0 + a1);
-        m = mn;
-        tmem_st64(tP, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(c, kBarPFull + w));
-    }
-    if (!ok || !mbar_wait(bar(c, kBarODone + w), (c.ntiles - 1) & 1, err))
-        return;
-    __syncwarp();
-    tc_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (write) {
+            // out[row, head*64 + d] = O / l, rounded to bf16; rows past the
+            // end of the sequence are not written
+            const int qpos = s.q0 + rr;
+            if (qpos < s.L) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<long long>(s.row0 + qpos) * kHidden
+                                                       + s.head * kHeadDim);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32 * h, o);
-        tmem_wait_ld();
-        uint32_t wv[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            wv[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-        if (qpos < c.L) {
-            uint4 *dst = reinterpret_cast<uint4 *>(out + static_cast<long long>(c.row0 + qpos) * kHidden
-                                                   + c.head * kHeadDim + 32 * h);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                for (int i = 0; i < kHeadDim / 8; ++i)
+                    dst[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
+                                        pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                                        pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                                        pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+            }
         }
     }
 }
@@ -336,43 +534,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
                    const __grid_constant__ CUtensorMap tm_qkv,
                    const int32_t *__restrict__ cu, const int2 *__restrict__ work,
-                   const int32_t *__restrict__ work_count, __nv_bfloat16 *__restrict__ out,
-                   int32_t *err)
+                   const int32_t *__restrict__ work_count, const int32_t *__restrict__ tile_start,
+                   int32_t *__restrict__ unit_cnt, float *__restrict__ partials,
+                   __nv_bfloat16 *__restrict__ out, int32_t *err)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     Ctx c;
     c.base = (raw + 1023u) & ~1023u;
-    uint32_t *slot = reinterpret_cast<uint32_t *>(smem_raw + (c.base - raw) + kOffSlot);
+    c.sbase = smem_raw + (c.base - raw);
+    uint32_t *slot = reinterpret_cast<uint32_t *>(c.sbase + kOffSlot);
 
-    const int entry = blockIdx.x / kHeads;
-    c.head = blockIdx.x % kHeads;
-    if (entry >= *work_count)
+    Params p;
+    p.entries = *work_count;
+    if (p.entries <= 0)
         return;
-    const int2 e = work[entry];
-    c.row0 = cu[e.x];
-    c.L = cu[e.x + 1] - c.row0;
-    c.q0 = e.y * 2 * kBlockM;
-    c.ntiles = (c.L + kBlockN - 1) / kBlockN;
+    p.cu = cu;
+    p.work = work;
+    p.tile_start = tile_start;
+    p.unit_cnt = unit_cnt;
+    p.partials = partials;
+    p.out = out;
+    p.err = err;
+    p.total = tile_start[p.entries];
+    // split among at most `total` CTAs, so that every range is non-empty
+    p.ctas = p.total < gridDim.x ? static_cast<int>(p.total) : static_cast<int>(gridDim.x);
+    const int cta = blockIdx.x;
+    if (cta >= p.ctas)
+        return;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tm_rot);
         tma_prefetch_desc(&tm_qkv);
-        mbar_init(bar(c, kBarQ), 1);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(bar(c, kBarQFull + q), 1);
+            mbar_init(bar(c, kBarQEmpty + q), 2);   // one commit per issuer
+        }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(c, kBarKFull + s), 1);
-            mbar_init(bar(c, kBarKEmpty + s), 1);
+            mbar_init(bar(c, kBarKEmpty + s), 2);
             mbar_init(bar(c, kBarVFull + s), 1);
-            mbar_init(bar(c, kBarVEmpty + s), 1);
+            mbar_init(bar(c, kBarVEmpty + s), 2);
         }
         for (int w = 0; w < 2; ++w) {
             mbar_init(bar(c, kBarSFull + w), 1);
             mbar_init(bar(c, kBarSEmpty + w), kBlockM);
             mbar_init(bar(c, kBarPFull + w), kBlockM);
             mbar_init(bar(c, kBarODone + w), 1);
+            mbar_init(bar(c, kBarOFree + w), kBlockM);
         }
+        mbar_init(bar(c, kBarSegSync), 2 * kBlockM);
+        mbar_init(bar(c, kBarSegFlag), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -388,15 +602,16 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsControl));
         if (warp == 8) {
             if (lane == 0)
-                producer(c, &tm_rot, &tm_qkv, err);
+                producer(c, p, &tm_rot, &tm_qkv, cta);
             __syncwarp();
-        } else if (warp == 9) {
-            mma_issuer(c, err);
+        } else if (warp == 9 || warp == 10) {
+            mma_issuer(c, p, warp - 9, cta);
             __syncwarp();
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegsSoftmax));
-        softmax_group(c, warp >> 2, warp & 3, lane, out, err);
+        softmax_group(c, p, warp >> 2, warp & 3, lane, cta);
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -422,9 +637,9 @@ cudaError_t launch_attn_global(const AttnArgs &a, cudaStream_t stream)
             return e;
         configured[dev] = true;
     }
-    const long long grid = static_cast<long long>(a.entry_bound) * kHeads;
-    attn_global_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
-        a.tm_rot, a.tm_qkv, a.cu, a.work, a.work_count, a.out, a.err);
+    attn_global_kernel<<<a.num_ctas, kThreads, kSmemBytes, stream>>>(
+        a.tm_rot, a.tm_qkv, a.cu, a.work, a.work_count, a.tile_start, a.unit_cnt, a.partials,
+        a.out, a.err);
     return cudaGetLastError();
 }
 

@@ -134,6 +134,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a waiting warp sleeps in hardware until
+// the phase completes (or about `hint_ns` pass) instead of re-polling, so it
+// takes no issue slots from the warps that share its SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up once
 // `limit_ns` of global time or 2.5 * limit_ns SM cycles have passed
 // (whichever comes first, so that the wait ends even if one clock stalls),
@@ -146,11 +160,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *er
     const unsigned long long t0 = globaltimer_ns();
     const long long c0 = clock64();
     const long long climit = static_cast<long long>(limit_ns) * 5 / 2;
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 1000000u))
             return true;
-        if ((it & 63u) == 0 &&
-            (globaltimer_ns() - t0 > limit_ns || clock64() - c0 > climit))
+        if (globaltimer_ns() - t0 > limit_ns || clock64() - c0 > climit)
             break;
     }
     atomicOr(err, kErrTimeout);

@@ -32,6 +32,12 @@ struct mbert_attn {
     int64_t work_cap = 0;                   // entries
     __nv_bfloat16 *rot = nullptr;           // rotated Q/K scratch [rows][1536]
     int64_t rot_cap = 0;                    // rows
+    // global layers: split of the (entry, head, key tile) iterations among
+    // one persistent CTA per SM
+    int32_t *tile_start = nullptr;          // [entries + 1]
+    int32_t *unit_cnt = nullptr;            // [entries * heads]
+    int64_t sk_cap = 0;                     // entries
+    float *partials = nullptr;              // [2 * num_sms][kPartialFloats]
     cudaStream_t last_stream = nullptr;
     EncodeTiledFn encode = nullptr;
     // measurement: event pairs around the attention kernel, per layer kind
@@ -87,6 +93,33 @@ int grow_workspace(mbert_attn *h, int64_t entries, int64_t rot_rows)
         }
         h->work = w;
         h->work_cap = cap;
+    }
+    // global-layer split bookkeeping, sized for 256-row entries (at most
+    // `entries` of them: (T + 255 n) / 256 <= the 128-row bound)
+    if (entries > h->sk_cap) {
+        int64_t cap = entries < 1024 ? 1024 : entries;
+        int32_t *ts = nullptr, *uc = nullptr;
+        if (cudaMalloc(&ts, sizeof(int32_t) * (cap + 1)) != cudaSuccess ||
+            cudaMalloc(&uc, sizeof(int32_t) * cap * kHeads) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(ts);
+            return MBERT_ERR_OOM;
+        }
+        if (h->tile_start) {
+            cudaDeviceSynchronize();
+            cudaFree(h->tile_start);
+            cudaFree(h->unit_cnt);
+        }
+        h->tile_start = ts;
+        h->unit_cnt = uc;
+        h->sk_cap = cap;
+    }
+    if (!h->partials) {
+        if (cudaMalloc(&h->partials, sizeof(float) * 2 * h->num_sms * kPartialFloats) != cudaSuccess) {
+            cudaGetLastError();
+            h->partials = nullptr;
+            return MBERT_ERR_OOM;
+        }
     }
     if (rot_rows > h->rot_cap) {
         int64_t cap = rot_rows < 8192 ? 8192 : rot_rows;
@@ -202,6 +235,9 @@ MBERT_API void mbert_attn_destroy(mbert_attn *h)
         cudaFree(h->work_count);
         cudaFree(h->work);
         cudaFree(h->rot);
+        cudaFree(h->tile_start);
+        cudaFree(h->unit_cnt);
+        cudaFree(h->partials);
     }
     delete h;
 }
@@ -332,9 +368,12 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
         return rc;
     Plan p = make_plan(h, cu_seqlens, n_seqs, T, max_seqlen);
     if (layer_kind == MBERT_GLOBAL) {
-        // the global kernel takes 256 query rows (two 128-row tiles) per entry
+        // the global kernel takes 256 query rows (two 128-row tiles) per
+        // entry and splits all iterations evenly among one CTA per SM
         p.block = 2 * kBlockM;
         p.entry_bound = static_cast<int>((T + (p.block - 1) * static_cast<int64_t>(n_seqs)) / p.block);
+        p.tile_start = h->tile_start;
+        p.unit_cnt = h->unit_cnt;
     }
 
     AttnArgs a;
@@ -348,6 +387,10 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
     a.half_window = layer_kind == MBERT_GLOBAL ? -1 : h->cfg.half_window;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.err = h->err;
+    a.num_ctas = h->num_sms;
+    a.tile_start = h->tile_start;
+    a.unit_cnt = h->unit_cnt;
+    a.partials = h->partials;
 
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     if (h->profiling) {

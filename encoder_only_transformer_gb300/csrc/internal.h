@@ -21,6 +21,12 @@ struct Plan {
     int32_t *work_count;    // device scalar: entries written (0 if the checks failed)
     int entry_bound;        // host-side upper bound on the entry count
     int32_t *err;           // device error word (sticky, bit mask)
+    // Optional (global layers): tile_start[e] = sum over entries before e of
+    // heads * ceil(L/128) (the entry's first iteration in the split of all
+    // (entry, head, key tile) iterations among persistent CTAs), with
+    // tile_start[count] = the total; unit_cnt[entry * heads + head] zeroed.
+    int32_t *tile_start = nullptr;   // device [entry_bound + 1]
+    int32_t *unit_cnt = nullptr;     // device [entry_bound * heads]
 };
 
 cudaError_t launch_plan(const Plan &p, cudaStream_t stream);
@@ -44,7 +50,17 @@ struct AttnArgs {
     int half_window;        // < 0: global layer
     __nv_bfloat16 *out;     // [T][768]
     int32_t *err;
+    // global layers: persistent CTAs and the split of iterations
+    int num_ctas = 0;
+    const int32_t *tile_start = nullptr;
+    int32_t *unit_cnt = nullptr;
+    float *partials = nullptr;   // [2 * num_ctas][kPartialFloats]
 };
+
+// One partial state of a query block split across CTAs: O (unnormalised,
+// fp32) for 256 rows x 64, then (m, l) for the 256 rows.
+constexpr int kPartialRows = 256;
+constexpr int kPartialFloats = kPartialRows * 64 + kPartialRows * 2;
 
 // One bounded mbarrier wait that nothing completes (exercises kErrTimeout).
 cudaError_t launch_wait_timeout_selftest(int32_t *err, unsigned long long limit_ns,

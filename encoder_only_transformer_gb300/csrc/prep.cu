@@ -46,7 +46,8 @@ __device__ int block_inclusive_scan(int v, int *warp_sums)
 // does not affect any result).
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seqlen, int blk,
-            int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count)
+            int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count,
+            int32_t *__restrict__ tile_start, int32_t *__restrict__ unit_cnt)
 {
     __shared__ int s_bad;
     __shared__ int s_hist[kMaxBins + 1];
@@ -104,6 +105,36 @@ plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seq
         for (int q = 0; q < nb; ++q)
             dst[q] = make_int2(s, q);
     }
+    if (tile_start == nullptr)
+        return;
+    // Iteration offsets of the entries, in list order: an exclusive scan of
+    // heads * ceil(L/128) (one iteration per head and key tile).
+    __syncthreads();
+    __shared__ int s_carry;
+    const int total = *work_count;
+    if (tid == 0)
+        s_carry = 0;
+    __syncthreads();
+    for (int b = 0; b < total; b += kPlanThreads) {
+        const int e = b + tid;
+        int v = 0;
+        if (e < total) {
+            const int2 w = work[e];
+            const int L = cu[w.x + 1] - cu[w.x];
+            v = kHeads * ((L + kBlockN - 1) / kBlockN);
+        }
+        const int incl = block_inclusive_scan(v, s_warp);
+        if (e < total)
+            tile_start[e] = s_carry + incl - v;
+        __syncthreads();
+        if (tid == kPlanThreads - 1)
+            s_carry += incl;
+        __syncthreads();
+    }
+    if (tid == 0)
+        tile_start[total] = s_carry;
+    for (int i = tid; i < total * kHeads; i += kPlanThreads)
+        unit_cnt[i] = 0;
 }
 
 // Sequence index of packed row `row` (cu validated, non-decreasing).
@@ -226,7 +257,8 @@ cudaError_t launch_wait_timeout_selftest(int32_t *err, unsigned long long limit_
 cudaError_t launch_plan(const Plan &p, cudaStream_t stream)
 {
     plan_kernel<<<1, kPlanThreads, 0, stream>>>(p.cu, p.n_seqs, p.T, p.max_seqlen, p.block,
-                                                  p.err, p.work, p.work_count);
+                                                  p.err, p.work, p.work_count, p.tile_start,
+                                                  p.unit_cnt);
     return cudaGetLastError();
 }
 

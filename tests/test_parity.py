@@ -138,15 +138,27 @@ def test_config5_layer_sampled(attn, layer):
 # properties that hold at any size
 # ---------------------------------------------------------------------------
 
+def _same(a, b, kind):
+    """Local layers process each sequence on its own: bit-identical.  The
+    global kernel splits the whole batch's work evenly among the SMs, so
+    where a sequence's work is cut (and partial results merged) depends on
+    the rest of the pack: equal up to rounding."""
+    if kind == "local":
+        assert torch.equal(a, b)
+    else:
+        d = (a.double() - b.double()).abs()
+        assert d.max().item() <= 1e-2 and d.mean().item() <= 1e-4
+
+
 @pytest.mark.parametrize("kind", ["global", "local"])
 def test_pad_sequence_leaves_real_rows_unchanged(attn, kind):
     """A padded token packed as its own sequence does not change the real
-    outputs (gap 0, bit for bit)."""
+    outputs (gap 0)."""
     real = W.custom([300, 41], seed=9)
     padded = W.custom([300, 41, 5], seed=9)
     a = _run(attn, real, kind)
     b = _run(attn, padded, kind)
-    assert torch.equal(a, b[:341])
+    _same(a, b[:341], kind)
 
 
 @pytest.mark.parametrize("kind", ["global", "local"])
@@ -157,7 +169,7 @@ def test_offset_in_pack_does_not_matter(attn, kind):
                       W.cu_from_lengths([150, 333]))
     alone = _run(attn, a, kind)
     packed = _run(attn, pack, kind)
-    assert torch.equal(alone, packed[150:])
+    _same(alone, packed[150:], kind)
 
 
 @pytest.mark.parametrize("kind", ["global", "local"])
