@@ -76,6 +76,33 @@ __device__ __forceinline__ bool admitted(int i, int j, int L, int hw)
 }
 
 // ---------------------------------------------------------------------------
+// local-band schedule (shared by the local attention and key-count kernels)
+//
+// A block of 128 queries at position q0 sees keys in [q0 - hw, q0 + 127 + hw];
+// for hw <= 64 two 128-key tiles cover that: tile 0 = keys q0 - 64 .. q0 + 63,
+// tile 1 = keys q0 + 64 .. q0 + 191.  Warp w (queries q0 + 32w .. + 31)
+// visits only the 32-key chunks of a tile that can hold a key within 64 of
+// one of its queries: chunks w..3 of tile 0 and chunks 0..w of tile 1
+// (5 chunks, 160 keys, per row instead of 256).
+// ---------------------------------------------------------------------------
+constexpr int kBandReach = 64;   // tile geometry supports half windows up to this
+
+__device__ __forceinline__ int band_tile_key0(int q0, int tile) { return q0 - 64 + 128 * tile; }
+__device__ __forceinline__ int band_chunk_begin(int tile, int w) { return tile == 0 ? w : 0; }
+__device__ __forceinline__ int band_chunk_end(int tile, int w) { return tile == 0 ? 4 : w + 1; }
+
+// Must chunk c of `tile` be masked element by element for warp w?  Not when
+// every key of the chunk lies in the sequence and within hw (= 64) of every
+// query of the warp: off-diagonal chunks of interior blocks.
+__device__ __forceinline__ bool band_chunk_needs_mask(int q0, int L, int hw, int tile, int w, int c)
+{
+    const int k0 = band_tile_key0(q0, tile) + 32 * c;
+    if (k0 < 0 || k0 + 31 >= L || hw != kBandReach)
+        return true;
+    return c == w;
+}
+
+// ---------------------------------------------------------------------------
 // small PTX helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p)

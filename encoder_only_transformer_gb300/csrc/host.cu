@@ -23,6 +23,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 struct mbert_attn {
     int device = 0;
+    RopeConsts rope_consts[2];              // per layer kind, for in-kernel cos/sin
     int num_sms = 0;
     mbert_attn_config cfg{};
     float2 *rope[2] = {nullptr, nullptr};   // [MBERT_GLOBAL], [MBERT_LOCAL]: [max_seqlen][32]
@@ -316,6 +317,23 @@ MBERT_API int mbert_attn_create(mbert_attn **out, const mbert_attn_config *cfg, 
             rc = MBERT_ERR_CUDA;
     }
     std::free(host);
+    // Constants for the kernels that compute cos/sin themselves: turns per
+    // position 1/(2 pi) base^(-2m/64) split into an 11-significant-bit high
+    // part and the remainder, and the rotation by 128 positions.
+    for (int k = 0; k < 2; ++k) {
+        for (int m = 0; m < kPairs; ++m) {
+            const double w = std::pow(thetas[k], -2.0 * m / kHeadDim);
+            const double turns = w / (2.0 * 3.14159265358979323846);
+            int e = 0;
+            std::frexp(turns, &e);                       // turns = f * 2^e, f in [0.5, 1)
+            const double q = std::ldexp(1.0, e - 11);    // keep 11 significant bits
+            const double hi = std::floor(turns / q) * q;
+            h->rope_consts[k].turns_hi[m] = static_cast<float>(hi);
+            h->rope_consts[k].turns_lo[m] = static_cast<float>(turns - hi);
+            h->rope_consts[k].cos128[m] = static_cast<float>(std::cos(128.0 * w));
+            h->rope_consts[k].sin128[m] = static_cast<float>(std::sin(128.0 * w));
+        }
+    }
     if (rc == MBERT_OK) {
         if (cudaMalloc(&h->err, sizeof(int32_t)) != cudaSuccess ||
             cudaMalloc(&h->work_count, sizeof(int32_t)) != cudaSuccess)
@@ -405,7 +423,40 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
         ev1 = v[h->ev_used[layer_kind] + 1];
         h->ev_used[layer_kind] += 2;
     }
-    cudaError_t e = launch_plan(p, st);
+    cudaError_t e = cudaSuccess;
+    if (layer_kind == MBERT_LOCAL && h->cfg.half_window <= kBandReach) {
+        // RoPE inside the attention kernel; with few sequences each CTA finds
+        // its block itself and no plan kernel runs.
+        LocalArgs la;
+        la.rope = h->rope_consts[MBERT_LOCAL];
+        la.tm_qkv = a.tm_qkv;
+        la.cu = cu_seqlens;
+        la.n_seqs = n_seqs;
+        la.T = T;
+        la.max_seqlen = p.max_seqlen;
+        la.half_window = h->cfg.half_window;
+        la.out = a.out;
+        la.err = h->err;
+        la.work = nullptr;
+        la.work_count = nullptr;
+        la.block_bound = p.entry_bound;
+        if (n_seqs > kLocalSelfScheduleMaxSeqs) {
+            e = launch_plan(p, st);
+            la.work = h->work;
+            la.work_count = h->work_count;
+            h->launches += 1;
+        }
+        if (e == cudaSuccess && ev0)
+            e = cudaEventRecord(ev0, st);
+        if (e == cudaSuccess)
+            e = launch_attn_local(la, st);
+        if (e == cudaSuccess && ev1)
+            e = cudaEventRecord(ev1, st);
+        h->launches += 1;
+        h->last_stream = st;
+        return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
+    }
+    e = launch_plan(p, st);
     if (e == cudaSuccess)
         e = launch_rope_qk(p, static_cast<const __nv_bfloat16 *>(qkv), h->rope[layer_kind],
                            h->cfg.max_seqlen, h->rot, st);

@@ -9,6 +9,8 @@
 
 namespace mbert {
 
+constexpr int kPairsConst = 32;
+
 // Work list written by the plan kernel: one entry per (sequence, 128-query
 // block), longest sequences first; the attention grid covers entries x heads.
 struct Plan {
@@ -61,6 +63,40 @@ struct AttnArgs {
 // fp32) for 256 rows x 64, then (m, l) for the 256 rows.
 constexpr int kPartialRows = 256;
 constexpr int kPartialFloats = kPartialRows * 64 + kPartialRows * 2;
+
+// RoPE constants for computing cos/sin in the kernel: for pair m the
+// frequency in turns per position, split into a high part with at most 11
+// significant bits (so that position * high is exact in fp32) and the rest,
+// and the rotation by 128 positions.
+struct RopeConsts {
+    float turns_hi[kPairsConst];
+    float turns_lo[kPairsConst];
+    float cos128[kPairsConst];
+    float sin128[kPairsConst];
+};
+
+struct LocalArgs {
+    RopeConsts rope;
+    CUtensorMap tm_qkv;          // qkv [T][2304], box 64 x 128, 128B swizzle
+    const int32_t *cu;
+    int n_seqs;
+    long long T;
+    int max_seqlen;
+    const int2 *work;            // null: each CTA finds its block from cu_seqlens
+    const int32_t *work_count;
+    int half_window;             // <= kBandReach
+    int block_bound;             // grid = block_bound * heads
+    __nv_bfloat16 *out;
+    int32_t *err;
+};
+
+// Local-layer attention with RoPE in the prologue: one CTA per (128-query
+// block, head), two band tiles of keys.
+cudaError_t launch_attn_local(const LocalArgs &a, cudaStream_t stream);
+
+// Number of sequences up to which the local kernel finds its blocks itself
+// (above it the plan kernel writes a work list first).
+constexpr int kLocalSelfScheduleMaxSeqs = 256;
 
 // One bounded mbarrier wait that nothing completes (exercises kErrTimeout).
 cudaError_t launch_wait_timeout_selftest(int32_t *err, unsigned long long limit_ns,

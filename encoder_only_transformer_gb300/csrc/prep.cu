@@ -216,16 +216,34 @@ key_count_kernel(const int32_t *__restrict__ cu, const int2 *__restrict__ work,
     const int L = cu[e.x + 1] - row0;
     const int q0 = e.y * kBlockM;
     const int qpos = q0 + threadIdx.x;
-    int kt0, kt1;
-    key_tile_range(q0, L, hw, kt0, kt1);
     int cnt = 0;
-    for (int kt = kt0; kt < kt1; ++kt) {
-        if (!tile_needs_mask(q0, L, hw, kt)) {
-            cnt += kBlockN;
-            continue;
+    if (hw >= 0 && hw <= kBandReach) {
+        // the local kernel: two band tiles, chunks chosen per warp
+        const int w = threadIdx.x >> 5;
+        for (int t = 0; t < 2; ++t) {
+            const int key0 = band_tile_key0(q0, t);
+            for (int c = band_chunk_begin(t, w); c < band_chunk_end(t, w); ++c) {
+                if (!band_chunk_needs_mask(q0, L, hw, t, w, c)) {
+                    cnt += 32;
+                    continue;
+                }
+                for (int k = 0; k < 32; ++k) {
+                    const int kp = key0 + 32 * c + k;
+                    cnt += (kp >= 0 && kp < L && abs(qpos - kp) <= hw) ? 1 : 0;
+                }
+            }
         }
-        for (int c = 0; c < kBlockN; ++c)
-            cnt += admitted(qpos, kt * kBlockN + c, L, hw) ? 1 : 0;
+    } else {
+        int kt0, kt1;
+        key_tile_range(q0, L, hw, kt0, kt1);
+        for (int kt = kt0; kt < kt1; ++kt) {
+            if (!tile_needs_mask(q0, L, hw, kt)) {
+                cnt += kBlockN;
+                continue;
+            }
+            for (int c = 0; c < kBlockN; ++c)
+                cnt += admitted(qpos, kt * kBlockN + c, L, hw) ? 1 : 0;
+        }
     }
     if (qpos < L)
         counts[row0 + qpos] = cnt;
