@@ -80,13 +80,6 @@ constexpr uint32_t kIdescO = make_idesc_bf16(128, 64, true);
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 
-__device__ __forceinline__ float fmax3(float a, float b, float c)
-{
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
 // (a0, a1) * (b, b) + (c, c) on the packed fp32x2 path
 __device__ __forceinline__ void ffma2_bc(float &x0, float &x1, float b, float c)
 {

@@ -423,7 +423,25 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 #undef MBERT_W8
 
+// Ties 32 registers to this point of the program: code that reads them is not
+// scheduled above an earlier tcgen05.wait::ld (the load's destination
+// registers are only valid after that wait).
+#define MBERT_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
+                     "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32])
+{
+    asm volatile("" : MBERT_RW8(0), MBERT_RW8(8), MBERT_RW8(16), MBERT_RW8(24));
+}
+#undef MBERT_RW8
+
 // ---- math ----
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;

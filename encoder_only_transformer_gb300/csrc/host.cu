@@ -318,18 +318,17 @@ MBERT_API int mbert_attn_create(mbert_attn **out, const mbert_attn_config *cfg, 
     }
     std::free(host);
     // Constants for the kernels that compute cos/sin themselves: turns per
-    // position 1/(2 pi) base^(-2m/64) split into an 11-significant-bit high
-    // part and the remainder, and the rotation by 128 positions.
+    // position, 1/(2 pi) base^(-2m/64), as a 64-bit binary fraction, and the
+    // rotation by 128 positions.
     for (int k = 0; k < 2; ++k) {
         for (int m = 0; m < kPairs; ++m) {
             const double w = std::pow(thetas[k], -2.0 * m / kHeadDim);
-            const double turns = w / (2.0 * 3.14159265358979323846);
-            int e = 0;
-            std::frexp(turns, &e);                       // turns = f * 2^e, f in [0.5, 1)
-            const double q = std::ldexp(1.0, e - 11);    // keep 11 significant bits
-            const double hi = std::floor(turns / q) * q;
-            h->rope_consts[k].turns_hi[m] = static_cast<float>(hi);
-            h->rope_consts[k].turns_lo[m] = static_cast<float>(turns - hi);
+            const double turns = w / (2.0 * 3.14159265358979323846);   // in (0, 1)
+            const double t32 = std::ldexp(turns, 32);
+            const double hi = std::floor(t32);
+            const double lo = std::floor(std::ldexp(t32 - hi, 32));
+            h->rope_consts[k].frac_hi[m] = static_cast<uint32_t>(hi);
+            h->rope_consts[k].frac_lo[m] = static_cast<uint32_t>(lo);
             h->rope_consts[k].cos128[m] = static_cast<float>(std::cos(128.0 * w));
             h->rope_consts[k].sin128[m] = static_cast<float>(std::sin(128.0 * w));
         }
@@ -440,6 +439,7 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
         la.work = nullptr;
         la.work_count = nullptr;
         la.block_bound = p.entry_bound;
+        la.num_ctas = h->num_sms;
         if (n_seqs > kLocalSelfScheduleMaxSeqs) {
             e = launch_plan(p, st);
             la.work = h->work;

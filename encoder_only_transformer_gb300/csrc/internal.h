@@ -65,12 +65,13 @@ constexpr int kPartialRows = 256;
 constexpr int kPartialFloats = kPartialRows * 64 + kPartialRows * 2;
 
 // RoPE constants for computing cos/sin in the kernel: for pair m the
-// frequency in turns per position, split into a high part with at most 11
-// significant bits (so that position * high is exact in fp32) and the rest,
-// and the rotation by 128 positions.
+// frequency in turns per position as a 64-bit binary fraction (frac_hi holds
+// 2^-1 .. 2^-32, frac_lo 2^-33 .. 2^-64), so that the turns of any position
+// are exact modulo 1 in integer arithmetic, and the rotation by 128
+// positions.
 struct RopeConsts {
-    float turns_hi[kPairsConst];
-    float turns_lo[kPairsConst];
+    uint32_t frac_hi[kPairsConst];
+    uint32_t frac_lo[kPairsConst];
     float cos128[kPairsConst];
     float sin128[kPairsConst];
 };
@@ -85,13 +86,15 @@ struct LocalArgs {
     const int2 *work;            // null: each CTA finds its block from cu_seqlens
     const int32_t *work_count;
     int half_window;             // <= kBandReach
-    int block_bound;             // grid = block_bound * heads
+    int block_bound;             // upper bound on 128-query blocks over all sequences
+    int num_ctas;                // persistent CTAs (one per SM)
     __nv_bfloat16 *out;
     int32_t *err;
 };
 
-// Local-layer attention with RoPE in the prologue: one CTA per (128-query
-// block, head), two band tiles of keys.
+// Local-layer attention with RoPE in the prologue: persistent CTAs, each
+// walking a contiguous range of (128-query block, head) units, two band
+// tiles of keys per unit.
 cudaError_t launch_attn_local(const LocalArgs &a, cudaStream_t stream);
 
 // Number of sequences up to which the local kernel finds its blocks itself
