@@ -80,26 +80,6 @@ constexpr uint32_t kIdescO = make_idesc_bf16(128, 64, true);
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 
-// (a0, a1) * (b, b) + (c, c) on the packed fp32x2 path
-__device__ __forceinline__ void ffma2_bc(float &x0, float &x1, float b, float c)
-{
-    uint64_t a, bb, cc, d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(x0), "f"(x1));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(bb), "l"(cc));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(d));
-}
-
-__device__ __forceinline__ void fadd2(float &a0, float &a1, float b0, float b1)
-{
-    uint64_t a, b, d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
-    asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(d));
-}
-
 // ---------------------------------------------------------------- schedule
 struct Params {
     const int32_t *cu;

@@ -5,9 +5,9 @@
 // (candding), "The alternating attention"), so for a block of 128 queries
 // starting at q0 every visible key lies in the 256-key window [q0 - 64,
 // q0 + 192), two 128-key tiles.  Query row r sees window columns
-// [r, r + 128]; warp w (rows 32w .. 32w + 31) therefore only ever needs the
-// five 32-key chunks starting at window column 32w, and never rescales: the
-// softmax of a row is taken in one go over its five chunks.
+// [r, r + 128]; the rows 32w .. 32w + 31 therefore only ever need the five
+// 32-key chunks starting at window column 32w, and the softmax of a row is
+// taken in one pass over them.
 //
 // Persistent: one CTA per SM walks a contiguous range of units (sequence,
 // 128-query block, head) in the order head, then work entry.  Consecutive
@@ -16,14 +16,17 @@
 // only Q and one new K/V tile.
 //
 //   warp 8      producer: TMA of raw Q, K, V tiles (16 KB, 128-byte swizzle)
-//               straight from the fused qkv rows into 4-deep rings
-//   warp 9      MMA issuer: S = Q [K0 K1]^T (256 TMEM columns), then, once
-//               softmax has written P, O = P0 V0 + P1 V1
-//   warps 0-3,  two compute groups taking alternate units: RoPE in shared
-//   warps 4-7   memory (rotate-half, positions restarting per sequence;
-//               "ModernBERT-base Architecture Teardown", "How Does RoPE Work
-//               With Two Bases?"), softmax (fp32, base 2) writing bf16 P over
-//               the S columns it has read, and the epilogue out = O / l
+//               straight from the fused qkv rows into rings (3 Q, 4 K, 4 V),
+//               and each unit's record (rows, block, head) beside its Q tile
+//   warps 9, 10 MMA issuers, one per compute group: S = Q [K0 K1]^T (256
+//               TMEM columns), then, once softmax has written P,
+//               O = P0 V0 + P1 V1
+//   warps 0-3,  two compute groups taking alternate units, one thread per
+//   warps 4-7   row: RoPE in shared memory (rotate-half, positions restarting
+//               per sequence; "ModernBERT-base Architecture Teardown", "How
+//               Does RoPE Work With Two Bases?"), softmax (fp32, base 2)
+//               writing bf16 P over the S columns already read, and the
+//               epilogue out = O / l through a staging tile and a TMA store
 //
 // TMEM: 512 columns, 256 per group: S over the window [0, 256); P0 packed
 // into [0, 64), P1 into [128, 192); O into [64, 128).
@@ -37,24 +40,36 @@
 namespace mbert {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kGroupThreads = 128;
+constexpr int kThreads = 352;
+constexpr int kGroupThreads = 128;     // 4 warps, one per TMEM lane quadrant
 constexpr int kWarpProducer = 8;
-constexpr int kWarpMma = 9;
-constexpr int kRing = 4;
+constexpr int kWarpMma = 9;            // + group: one MMA issuer per compute group
+constexpr int kQRing = 3;              // Q tiles
+constexpr int kRing = 4;               // K and V tiles
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kRing * kTileBytes;
-constexpr uint32_t kOffV = 2 * kRing * kTileBytes;
-constexpr uint32_t kOffBar = 3 * kRing * kTileBytes;
+constexpr uint32_t kOffK = kQRing * kTileBytes;
+constexpr uint32_t kOffV = kOffK + kRing * kTileBytes;
+constexpr uint32_t kOffStage = kOffV + kRing * kTileBytes;   // per group: O tile (bf16) for the TMA store
+constexpr uint32_t kOffRec = kOffStage + 2 * kTileBytes;    // per Q slot: the unit's record (32 bytes)
+constexpr uint32_t kOffPrev = kOffRec + kQRing * 32;         // per group: the unit awaiting its epilogue (16 bytes)
+constexpr uint32_t kOffBar = kOffRec + 128;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kGroupCols = 256;
 constexpr uint32_t kColO = 64;
 
+// Ring barriers (one per slot): full (TMA landed), empty (consumers done;
+// K and V take two arrivals per tile: one from each unit using it, or two
+// from a tile's only user), rotated (RoPE done; Q and K).  Per group: S
+// ready, P written, O ready, TMEM free (epilogue done), drain, staging tile
+// written (all rows), staging tile free (the previous TMA store has read
+// it).
 enum : int {
-    kBarQF = 0, kBarQE = 4, kBarKF = 8, kBarKE = 12, kBarVF = 16, kBarVE = 20,
-    kBarRope = 24, kBarS = 26, kBarP = 28, kBarO = 30, kBarFree = 32, kBarDrain = 34,
-    kNumBars = 35
+    kBarQF = 0, kBarQE = 3, kBarKF = 6, kBarKE = 10, kBarVF = 14, kBarVE = 18,
+    kBarQR = 22, kBarKR = 25,
+    kBarS = 29, kBarP = 31, kBarO = 33, kBarFree = 35, kBarDrain = 37,
+    kBarStg = 39, kBarStgFree = 41,
+    kNumBars = 43
 };
 
 constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false);
@@ -65,6 +80,7 @@ constexpr unsigned long long kDrainLimitNs = 100000000ull;
 
 __device__ __forceinline__ uint32_t barp(uint32_t base, int i) { return base + kOffBar + 8u * i; }
 __device__ __forceinline__ uint32_t ring_parity(int t) { return static_cast<uint32_t>(t / kRing) & 1u; }
+__device__ __forceinline__ uint32_t qring_parity(int k) { return static_cast<uint32_t>(k / kQRing) & 1u; }
 
 // Chunks j and j + 4 (elements 8j .. 8j + 7 and 32 + 8j .. 32 + 8j + 7, the
 // pairs m = 8j .. 8j + 7) of one 128-byte swizzled row (64 bf16): 16-byte
@@ -81,18 +97,24 @@ __device__ __forceinline__ void pair_load(uint32_t row_addr, int r, int j, PairC
     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.z[0]), "=r"(v.z[1]), "=r"(v.z[2]), "=r"(v.z[3]) : "r"(b));
 }
 
-// Rotate the pairs (x[m], x[m + 32]) by the angles whose cosines and sines
-// are c[m - 8j], s[m - 8j] and store the two chunks back.
+// Cosines and sines of eight pairs' angles, packed two pairs per register:
+// c[i] = (cos, cos) of pairs 2i, 2i + 1; s[i] the sines; ns[i] = -s[i].
+struct Angles8 {
+    uint64_t c[4], s[4], ns[4];
+};
+
+// Rotate the pairs (x[m], x[m + 32]) of the chunk pair j by the angles in
+// `an`: x' = x cos - z sin, z' = z cos + x sin (fp32), and store the two
+// chunks back.
 __device__ __forceinline__ void pair_rotate_store(uint32_t row_addr, int r, int j, const PairChunks &v,
-                                                  const float (&c)[8], const float (&s)[8])
+                                                  const Angles8 &an)
 {
     uint32_t ya[4], yb[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float x0 = bf16lo_to_f32(v.x[i]), x1 = bf16hi_to_f32(v.x[i]);
-        const float z0 = bf16lo_to_f32(v.z[i]), z1 = bf16hi_to_f32(v.z[i]);
-        ya[i] = pack_bf16x2(x0 * c[2 * i] - z0 * s[2 * i], x1 * c[2 * i + 1] - z1 * s[2 * i + 1]);
-        yb[i] = pack_bf16x2(z0 * c[2 * i] + x0 * s[2 * i], z1 * c[2 * i + 1] + x1 * s[2 * i + 1]);
+        const uint64_t x = bf16x2_to_f2(v.x[i]), z = bf16x2_to_f2(v.z[i]);
+        ya[i] = f2_to_bf16x2(ffma2(z, an.ns[i], fmul2(x, an.c[i])));
+        yb[i] = f2_to_bf16x2(ffma2(z, an.c[i], fmul2(x, an.s[i])));
     }
     const uint32_t a = row_addr + ((j ^ (r & 7)) << 4);
     const uint32_t b = row_addr + (((j + 4) ^ (r & 7)) << 4);
@@ -255,7 +277,8 @@ struct Walker {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ RopeConsts rope,
+attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_out,
+                  const __grid_constant__ RopeConsts rope,
                   const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seqlen,
                   const int2 *__restrict__ work, const int32_t *__restrict__ work_count, int hw,
                   __nv_bfloat16 *__restrict__ out, int32_t *err)
@@ -301,10 +324,13 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
     }
     if (tid == 32) {
         tma_prefetch_desc(&tm_qkv);
+        tma_prefetch_desc(&tm_out);
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == kBarRope || i == kBarRope + 1 || i == kBarP || i == kBarP + 1 ||
-                i == kBarFree || i == kBarFree + 1)
+            if ((i >= kBarKE && i < kBarKE + kRing) || (i >= kBarVE && i < kBarVE + kRing))
+                count = 2;
+            if ((i >= kBarQR && i < kBarKR + kRing) || i == kBarP || i == kBarP + 1 ||
+                i == kBarFree || i == kBarFree + 1 || i == kBarStg || i == kBarStg + 1)
                 count = kGroupThreads;
             mbar_init(barp(base, i), count);
         }
@@ -315,327 +341,426 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    Walker w;
-    w.start(cu, work, G, u_lo, s_first[1], s_first[2]);
+    if (warp >= kWarpProducer) {
+        if (warp == kWarpProducer) {
+            // ------------------------------------------------------ producer
+            Walker w;
+            w.start(cu, work, G, u_lo, s_first[1], s_first[2]);
+            const uint64_t once = l2_policy_evict_first();
+            int nq = 0, tk = 0, tv = 0;   // tiles issued per ring (issued in index order)
+            bool ok = true;
+            // wait for the ring slot of tile t, then TMA the 128 x 64 box at
+            // (column x, row y) into it
+            auto load = [&](uint32_t ring_off, int nslots, int bar_full, int bar_empty, int t, int x, int y,
+                            int &issued) {
+                if (!ok)
+                    return;
+                const int sl = t % nslots;
+                const uint32_t par = static_cast<uint32_t>(t / nslots) & 1u;
+                if (!(ok = mbar_wait(barp(base, bar_empty + sl), par ^ 1u, err)))
+                    return;
+                if (elect_one_sync()) {
+                    mbar_arrive_expect_tx(barp(base, bar_full + sl), kTileBytes);
+                    tma_load_2d_hint(base + ring_off + sl * kTileBytes, &tm_qkv, x, y,
+                                     barp(base, bar_full + sl), once);
+                }
+                __syncwarp();
+                issued = t + 1;
+            };
+            // Q and K of unit k (needed first, by RoPE), then the V tiles of
+            // unit k - 1 (needed last, by P V); unit k is only started once the
+            // Q tile of unit k - 2 has landed, so that at the start every SM's
+            // first tiles are not queued behind a burst of prefetches.
+            int tc = 0, a_prev = 0, colV_prev = 0, r0_prev = 0;
+            bool fresh_prev = false;
+            for (int k = 0; k < nunits && ok; ++k) {
+                const int a = w.fresh ? tc : tc - 1;
+                tc = a + 2;
+                const int colQ = w.head * kHeadDim, colK = kHidden + colQ, colV = 2 * kHidden + colQ;
+                const int r0 = w.row0 + w.qb * kBlockM;
+                if (k >= 2)
+                    ok = mbar_wait(barp(base, kBarQF + (k - 2) % kQRing), qring_parity(k - 2), err);
+                if (w.fresh)
+                    load(kOffK, kRing, kBarKF, kBarKE, a, colK, r0 - 64, tk);
+                // the unit's record for the compute group, published with its Q
+                // tile (the slot is free once the Q slot is: S of unit k - 3 done)
+                if (ok && mbar_wait(barp(base, kBarQE + k % kQRing), qring_parity(k) ^ 1u, err)) {
+                    if (lane == 0) {
+                        const uint32_t rec = base + kOffRec + (k % kQRing) * 32;
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
+                                     :: "r"(rec), "r"(w.row0), "r"(w.L), "r"(w.qb * kBlockM), "r"(w.head) : "memory");
+                        asm volatile("st.shared.v2.b32 [%0], {%1,%2};"
+                                     :: "r"(rec + 16), "r"(w.fresh ? 1 : 0), "r"(a) : "memory");
+                    }
+                    __syncwarp();
+                } else {
+                    ok = false;
+                }
+                load(kOffQ, kQRing, kBarQF, kBarQE, k, colQ, r0, nq);
+                load(kOffK, kRing, kBarKF, kBarKE, a + 1, colK, r0 + 64, tk);
+                if (k >= 1) {
+                    if (fresh_prev)
+                        load(kOffV, kRing, kBarVF, kBarVE, a_prev, colV_prev, r0_prev - 64, tv);
+                    load(kOffV, kRing, kBarVF, kBarVE, a_prev + 1, colV_prev, r0_prev + 64, tv);
+                }
+                a_prev = a;
+                fresh_prev = w.fresh;
+                colV_prev = colV;
+                r0_prev = r0;
+                if (k + 1 < nunits)
+                    w.next();
+            }
+            if (fresh_prev)
+                load(kOffV, kRing, kBarVF, kBarVE, a_prev, colV_prev, r0_prev - 64, tv);
+            load(kOffV, kRing, kBarVF, kBarVE, a_prev + 1, colV_prev, r0_prev + 64, tv);
+            // every copy issued has landed before the CTA can exit
+            for (int t = max(0, nq - kQRing); t < nq; ++t)
+                mbar_wait(barp(base, kBarQF + t % kQRing), qring_parity(t), err, kDrainLimitNs);
+            for (int t = max(0, tk - kRing); t < tk; ++t)
+                mbar_wait(barp(base, kBarKF + t % kRing), ring_parity(t), err, kDrainLimitNs);
+            for (int t = max(0, tv - kRing); t < tv; ++t)
+                mbar_wait(barp(base, kBarVF + t % kRing), ring_parity(t), err, kDrainLimitNs);
+        } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+            // ------------------------------------------------------ MMA issuers
+            Walker w;
+            w.start(cu, work, G, u_lo, s_first[1], s_first[2]);
+            const int g = warp - kWarpMma;
+            const uint32_t tm = tmem + g * kGroupCols;
+            bool ok = true;
+            int tc = 0;
+            bool fresh = w.fresh;
+            // Each unit gives every K and V tile it uses one release; a tile that
+            // has no second user (tile 0 of a fresh unit, tile 1 when the next
+            // unit is fresh or there is none) gets both releases from it.
+            for (int k = 0; k < nunits && ok; ++k) {
+                const int a = fresh ? tc : tc - 1;
+                tc = a + 2;
+                bool fresh_next = true;
+                if (k + 1 < nunits) {
+                    w.next();
+                    fresh_next = w.fresh;
+                }
+                if ((k & 1) == g) {
+                    const int j = k >> 1;
+                    ok = mbar_wait(barp(base, kBarQR + k % kQRing), qring_parity(k), err) &&
+                         mbar_wait(barp(base, kBarKR + a % kRing), ring_parity(a), err) &&
+                         mbar_wait(barp(base, kBarKR + (a + 1) % kRing), ring_parity(a + 1), err) &&
+                         (j == 0 || mbar_wait(barp(base, kBarFree + g), static_cast<uint32_t>(j - 1) & 1u, err));
+                    if (!ok)
+                        break;
+                    __syncwarp();
+                    tc_fence_after();
+                    const uint32_t q = base + kOffQ + (k % kQRing) * kTileBytes;
+    #pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint32_t kt = base + kOffK + ((a + t) % kRing) * kTileBytes;
+    #pragma unroll
+                        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+                            mma_bf16_ss_warp(tm + 128 * t, make_sdesc_sw128(q + 32 * kk, 16, 1024),
+                                             make_sdesc_sw128(kt + 32 * kk, 16, 1024), kIdescS, kk > 0);
+                    }
+                    mma_commit_warp(barp(base, kBarS + g));
+                    mma_commit_warp(barp(base, kBarQE + k % kQRing));
+                    mma_commit_warp(barp(base, kBarKE + a % kRing));
+                    mma_commit_warp(barp(base, kBarKE + (a + 1) % kRing));
+                    if (fresh)
+                        mma_commit_warp(barp(base, kBarKE + a % kRing));
+                    if (fresh_next)
+                        mma_commit_warp(barp(base, kBarKE + (a + 1) % kRing));
 
-    if (warp == kWarpProducer) {
-        // ------------------------------------------------------ producer
-        const uint64_t once = l2_policy_evict_first();
-        int nq = 0, tk = 0, tv = 0;   // tiles issued per ring (issued in index order)
-        bool ok = true;
-        // wait for the ring slot of tile t, then TMA the 128 x 64 box at
-        // (column x, row y) into it
-        auto load = [&](uint32_t ring_off, int bar_full, int bar_empty, int t, int x, int y,
-                        int &issued) {
-            if (!ok)
-                return;
-            if (!(ok = mbar_wait(barp(base, bar_empty + t % kRing), ring_parity(t) ^ 1u, err)))
-                return;
-            if (elect_one_sync()) {
-                mbar_arrive_expect_tx(barp(base, bar_full + t % kRing), kTileBytes);
-                tma_load_2d_hint(base + ring_off + (t % kRing) * kTileBytes, &tm_qkv, x, y,
-                                 barp(base, bar_full + t % kRing), once);
+                    ok = mbar_wait(barp(base, kBarP + g), static_cast<uint32_t>(j) & 1u, err) &&
+                         mbar_wait(barp(base, kBarVF + a % kRing), ring_parity(a), err) &&
+                         mbar_wait(barp(base, kBarVF + (a + 1) % kRing), ring_parity(a + 1), err);
+                    if (!ok)
+                        break;
+                    __syncwarp();
+                    tc_fence_after();
+    #pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint32_t v = base + kOffV + ((a + t) % kRing) * kTileBytes;
+    #pragma unroll
+                        for (int kk = 0; kk < kBlockN / 16; ++kk)
+                            mma_bf16_ts_warp(tm + kColO, tm + 128 * t + 8 * kk,
+                                             make_sdesc_sw128(v + 2048 * kk, 1024, 1024), kIdescO,
+                                             (t > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit_warp(barp(base, kBarO + g));
+                    mma_commit_warp(barp(base, kBarVE + a % kRing));
+                    mma_commit_warp(barp(base, kBarVE + (a + 1) % kRing));
+                    if (fresh)
+                        mma_commit_warp(barp(base, kBarVE + a % kRing));
+                    if (fresh_next)
+                        mma_commit_warp(barp(base, kBarVE + (a + 1) % kRing));
+                }
+                fresh = fresh_next;
             }
-            __syncwarp();
-            issued = t + 1;
-        };
-        int tc = 0;
-        for (int k = 0; k < nunits && ok; ++k) {
-            const int a = w.fresh ? tc : tc - 1;
-            tc = a + 2;
-            const int colQ = w.head * kHeadDim, colK = kHidden + colQ, colV = 2 * kHidden + colQ;
-            const int r0 = w.row0 + w.qb * kBlockM;
-            if (w.fresh)
-                load(kOffK, kBarKF, kBarKE, a, colK, r0 - 64, tk);
-            load(kOffQ, kBarQF, kBarQE, k, colQ, r0, nq);
-            load(kOffK, kBarKF, kBarKE, a + 1, colK, r0 + 64, tk);
-            if (w.fresh)
-                load(kOffV, kBarVF, kBarVE, a, colV, r0 - 64, tv);
-            load(kOffV, kBarVF, kBarVE, a + 1, colV, r0 + 64, tv);
-            if (k + 1 < nunits)
-                w.next();
+            // every MMA issued has completed before TMEM is released
+            mma_commit_warp(barp(base, kBarDrain + g));
+            mbar_wait(barp(base, kBarDrain + g), 0, err, kDrainLimitNs);
         }
-        // every copy issued has landed before the CTA can exit
-        for (int t = max(0, nq - kRing); t < nq; ++t)
-            mbar_wait(barp(base, kBarQF + t % kRing), ring_parity(t), err, kDrainLimitNs);
-        for (int t = max(0, tk - kRing); t < tk; ++t)
-            mbar_wait(barp(base, kBarKF + t % kRing), ring_parity(t), err, kDrainLimitNs);
-        for (int t = max(0, tv - kRing); t < tv; ++t)
-            mbar_wait(barp(base, kBarVF + t % kRing), ring_parity(t), err, kDrainLimitNs);
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------ MMA issuer
-        bool ok = true;
-        int tc = 0;
-        int a_prev = 0, a_prev2 = 0;
-        bool fresh_prev = true;
-        // O = P0 V0 + P1 V1 of unit kp (tiles ap, ap + 1); a fresh unit that
-        // follows another also retires its predecessor's V tile 1.
-        auto issue_pv = [&](int kp, int ap, bool fresh_p, int ap_before) -> bool {
-            const int g = kp & 1;
-            const uint32_t tm = tmem + g * kGroupCols;
-            if (!(mbar_wait(barp(base, kBarP + g), static_cast<uint32_t>(kp >> 1) & 1u, err) &&
-                  mbar_wait(barp(base, kBarVF + ap % kRing), ring_parity(ap), err) &&
-                  mbar_wait(barp(base, kBarVF + (ap + 1) % kRing), ring_parity(ap + 1), err)))
-                return false;
-            __syncwarp();
-            tc_fence_after();
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const uint32_t v = base + kOffV + ((ap + t) % kRing) * kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_bf16_ts_warp(tm + kColO, tm + 128 * t + 8 * kk,
-                                     make_sdesc_sw128(v + 2048 * kk, 1024, 1024), kIdescO,
-                                     (t > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit_warp(barp(base, kBarO + g));
-            mma_commit_warp(barp(base, kBarVE + ap % kRing));
-            if (fresh_p && kp > 0)
-                mma_commit_warp(barp(base, kBarVE + (ap_before + 1) % kRing));
-            return true;
-        };
-        for (int k = 0; k < nunits && ok; ++k) {
-            const bool fresh = w.fresh;
-            const int a = fresh ? tc : tc - 1;
-            tc = a + 2;
-            const int g = k & 1, j = k >> 1;
-            const uint32_t tm = tmem + g * kGroupCols;
-            ok = mbar_wait(barp(base, kBarRope + g), static_cast<uint32_t>(j) & 1u, err) &&
-                 (j == 0 || mbar_wait(barp(base, kBarFree + g), static_cast<uint32_t>(j - 1) & 1u, err));
-            if (!ok)
-                break;
-            __syncwarp();
-            tc_fence_after();
-            const uint32_t q = base + kOffQ + (k % kRing) * kTileBytes;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const uint32_t kt = base + kOffK + ((a + t) % kRing) * kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk)
-                    mma_bf16_ss_warp(tm + 128 * t, make_sdesc_sw128(q + 32 * kk, 16, 1024),
-                                     make_sdesc_sw128(kt + 32 * kk, 16, 1024), kIdescS, kk > 0);
-            }
-            mma_commit_warp(barp(base, kBarS + g));
-            mma_commit_warp(barp(base, kBarQE + k % kRing));
-            mma_commit_warp(barp(base, kBarKE + a % kRing));
-            if (fresh && k > 0)
-                mma_commit_warp(barp(base, kBarKE + (a_prev + 1) % kRing));
-            if (k > 0)
-                ok = issue_pv(k - 1, a_prev, fresh_prev, a_prev2);
-            a_prev2 = a_prev;
-            a_prev = a;
-            fresh_prev = fresh;
-            if (k + 1 < nunits)
-                w.next();
-        }
-        if (ok)
-            issue_pv(nunits - 1, a_prev, fresh_prev, a_prev2);
-        // every MMA issued has completed before TMEM is released
-        mma_commit_warp(barp(base, kBarDrain));
-        mbar_wait(barp(base, kBarDrain), 0, err, kDrainLimitNs);
-    } else if (warp < 8) {
+    } else {
         // ------------------------------------------------------ compute groups
-        const int g = warp >> 2, wq = warp & 3;
-        const int r = 32 * wq + lane;                 // row in the block, TMEM lane
-        const uint32_t tm = tmem + g * kGroupCols + (static_cast<uint32_t>(32 * wq) << 16);
-        bool ok = true;
-        int tc = 0, j = 0;
+        // Warp q of group g (warp 4g + q): TMEM lane quadrant q, rows
+        // 32q .. 32q + 31, one row per thread.
+        const int g = warp >> 2, q = warp & 3;
+        const int r = 32 * q + lane;                  // row in the block, TMEM lane
+        const uint32_t tm = tmem + g * kGroupCols + (static_cast<uint32_t>(32 * q) << 16);
+        const uint32_t stage = base + kOffStage + g * kTileBytes;
         // the group's previous unit, whose epilogue runs after the next
-        // unit's RoPE (while its P V product is on the tensor cores)
-        int p_row = -1, p_col = 0;
-        float p_inv = 0.f;
+        // unit's RoPE (while its P V product is on the tensor cores): its
+        // rows, block and head in shared memory, its row sum in p_sum
+        const uint32_t prev = base + kOffPrev + g * 16;
+        const bool lead = r == 0;                     // issues the group's TMA stores
+        bool ok = true;
+        int j = 0, nst = 0;                           // units done; staged (TMA-stored) epilogues
+        float p_sum = 0.f;
 
+        // out = O / l.  A full block goes through the group's staging tile
+        // and one TMA store; a block that runs past its sequence end stores
+        // its rows directly (rows past the end are not written).
         auto epilogue = [&](int jp) -> bool {
-            if (!mbar_wait(barp(base, kBarO + g), static_cast<uint32_t>(jp) & 1u, err))
+            // P of the unit complete (its record is visible) and O = P V ready
+            if (!(mbar_wait(barp(base, kBarP + g), static_cast<uint32_t>(jp) & 1u, err) &&
+                  mbar_wait(barp(base, kBarO + g), static_cast<uint32_t>(jp) & 1u, err)))
                 return false;
             __syncwarp();
             tc_fence_after();
             uint32_t o[2][32];
             tmem_ld32(tm + kColO, o[0]);
             tmem_ld32(tm + kColO + 32, o[1]);
+            int row0, q0, L, head;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(row0), "=r"(q0), "=r"(L), "=r"(head) : "r"(prev) : "memory");
             tmem_wait_ld();
             reg_fence32(o[0]);
             reg_fence32(o[1]);
-            if (p_row >= 0) {
+            tc_fence_before();
+            mbar_arrive(barp(base, kBarFree + g));     // the group's TMEM may be reused
+            const int p_row = q0 + r < L ? row0 + q0 + r : -1;
+            const int p_col = head * kHeadDim;
+            const int p_blk = q0 + kBlockM <= L ? row0 + q0 : -1;     // a full block
+            const float inv = p_sum > 0.f ? 1.f / p_sum : 0.f;
+            uint32_t w4[8][4];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w4[c][e] = pack_bf16x2(__uint_as_float(o[c / 4][8 * (c % 4) + 2 * e]) * inv,
+                                           __uint_as_float(o[c / 4][8 * (c % 4) + 2 * e + 1]) * inv);
+            if (p_blk >= 0) {
+                const uint32_t par = static_cast<uint32_t>(nst) & 1u;
+                ++nst;
+                if (lead) {
+                    bulk_wait_read0();                  // the previous store has left the tile
+                    mbar_arrive(barp(base, kBarStgFree + g));
+                }
+                if (!mbar_wait(barp(base, kBarStgFree + g), par, err))
+                    return false;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
+                                 :: "r"(stage + r * 128 + ((c ^ (r & 7)) << 4)),
+                                    "r"(w4[c][0]), "r"(w4[c][1]), "r"(w4[c][2]), "r"(w4[c][3]) : "memory");
+                fence_proxy_async_smem();
+                mbar_arrive(barp(base, kBarStg + g));
+                if (lead) {
+                    if (!mbar_wait(barp(base, kBarStg + g), par, err))
+                        return false;
+                    tma_store_2d(&tm_out, stage, p_col, p_blk);
+                    bulk_commit();
+                }
+            } else if (p_row >= 0) {
                 uint4 *dst = reinterpret_cast<uint4 *>(out + static_cast<long long>(p_row) * kHidden + p_col);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t *x = o[k / 4] + 8 * (k % 4);
-                    dst[k] = make_uint4(
-                        pack_bf16x2(__uint_as_float(x[0]) * p_inv, __uint_as_float(x[1]) * p_inv),
-                        pack_bf16x2(__uint_as_float(x[2]) * p_inv, __uint_as_float(x[3]) * p_inv),
-                        pack_bf16x2(__uint_as_float(x[4]) * p_inv, __uint_as_float(x[5]) * p_inv),
-                        pack_bf16x2(__uint_as_float(x[6]) * p_inv, __uint_as_float(x[7]) * p_inv));
-                }
+                for (int c = 0; c < 8; ++c)
+                    dst[c] = make_uint4(w4[c][0], w4[c][1], w4[c][2], w4[c][3]);
             }
-            tc_fence_before();
-            mbar_arrive(barp(base, kBarFree + g));
             return true;
         };
 
-        for (int k = 0; k < nunits && ok; ++k) {
-            const bool fresh = w.fresh;
-            const int a = fresh ? tc : tc - 1;
-            tc = a + 2;
-            if ((k & 1) == g) {
-                const int q0 = w.qb * kBlockM, L = w.L;
-                // ---- RoPE.  Thread r takes position p = q0 + 64 + r: K
-                // tile 1 row r, and the Q row at p (r + 64, for r < 64) or
-                // at p - 128 (r - 64, for r >= 64), and on a fresh unit K
-                // tile 0 row r (at p - 128).  cos/sin at p - 128 come from
-                // those at p by one rotation of -128 positions.
-                ok = mbar_wait(barp(base, kBarQF + k % kRing), ring_parity(k), err) &&
-                     mbar_wait(barp(base, kBarKF + (a + 1) % kRing), ring_parity(a + 1), err) &&
-                     (!fresh || mbar_wait(barp(base, kBarKF + a % kRing), ring_parity(a), err));
-                if (ok) {
-                    const uint32_t qs = base + kOffQ + (k % kRing) * kTileBytes;
-                    const uint32_t k0s = base + kOffK + (a % kRing) * kTileBytes;
-                    const uint32_t k1s = base + kOffK + ((a + 1) % kRing) * kTileBytes;
-                    const uint32_t p = static_cast<uint32_t>(q0 + 64 + r);
-                    const bool q_at_p = r < 64;          // warp-uniform
-                    const int qr = q_at_p ? r + 64 : r - 64;
 #pragma unroll 1
-                    for (int jj = 0; jj < 4; ++jj) {
-                        // the rows' chunks first (one shared-memory round
-                        // trip), then the angles, then rotate and store
-                        PairChunks vk1, vq, vk0;
-                        pair_load(k1s + r * 128, r, jj, vk1);
-                        pair_load(qs + qr * 128, qr, jj, vq);
-                        if (fresh)
-                            pair_load(k0s + r * 128, r, jj, vk0);
-                        float c[8], s[8], cm[8], sm[8], cq[8], sq[8];
-#pragma unroll
-                        for (int kx = 0; kx < 8; ++kx) {
-                            const int m = 8 * jj + kx;
-                            pos_cos_sin(p, rope.frac_hi[m], rope.frac_lo[m], c[kx], s[kx]);
-                            cm[kx] = c[kx] * rope.cos128[m] + s[kx] * rope.sin128[m];
-                            sm[kx] = s[kx] * rope.cos128[m] - c[kx] * rope.sin128[m];
-                            cq[kx] = q_at_p ? c[kx] : cm[kx];
-                            sq[kx] = q_at_p ? s[kx] : sm[kx];
-                        }
-                        pair_rotate_store(k1s + r * 128, r, jj, vk1, c, s);
-                        pair_rotate_store(qs + qr * 128, qr, jj, vq, cq, sq);
-                        if (fresh)
-                            pair_rotate_store(k0s + r * 128, r, jj, vk0, cm, sm);
-                    }
-                    fence_proxy_async_smem();
-                }
-                mbar_arrive(barp(base, kBarRope + g));
-                if (!ok)
-                    break;
+        for (int k = g; k < nunits && ok; k += 2) {
+            // ---- the unit's record (published with its Q tile)
+            if (!(ok = mbar_wait(barp(base, kBarQF + k % kQRing), qring_parity(k), err)))
+                break;
+            const uint32_t rec = base + kOffRec + (k % kQRing) * 32;
+            int row0, L, q0, head, fresh_i, a;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(row0), "=r"(L), "=r"(q0), "=r"(head) : "r"(rec) : "memory");
+            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(fresh_i), "=r"(a) : "r"(rec + 16) : "memory");
+            const bool fresh = fresh_i != 0;
 
-                if (j > 0 && !(ok = epilogue(j - 1)))
-                    break;
-
-                // ---- softmax over the window chunks 32 wq .. 32 wq + 159
-                const int i = q0 + r;
-                // admitted keys [klo, khi]; none for rows past the sequence
-                const int klo = i < L ? max(0, i - hw) : L, khi = min(L - 1, i + hw);
-                if (!(ok = mbar_wait(barp(base, kBarS + g), static_cast<uint32_t>(j) & 1u, err)))
-                    break;
-                __syncwarp();
-                tc_fence_after();
-                // masked keys of chunk e (window columns 32 (wq + e) ..) ->
-                // -inf; only the edge chunks, chunks at a sequence edge or a
-                // narrower band have any
-                auto mask = [&](uint32_t (&x)[32], int e) {
-                    const int key0 = q0 - 64 + 32 * (wq + e);
-                    if (e == 0 || e == 4 || hw != kBandReach || key0 < 0 || key0 + 31 >= L) {
-                        const int lo = klo - key0, hi = khi - key0;
+            // ---- RoPE.  Thread r takes position p = q0 + 64 + r: K tile 1
+            // row r, and the Q row at p (r + 64, for r < 64) or at p - 128
+            // (r - 64, for r >= 64), and on a fresh unit K tile 0 row r (at
+            // p - 128).  cos/sin at p - 128 come from those at p by one
+            // rotation of -128 positions.
+            ok = mbar_wait(barp(base, kBarKF + (a + 1) % kRing), ring_parity(a + 1), err) &&
+                 (!fresh || mbar_wait(barp(base, kBarKF + a % kRing), ring_parity(a), err));
+            if (ok) {
+                const uint32_t qs = base + kOffQ + (k % kQRing) * kTileBytes;
+                const uint32_t k0s = base + kOffK + (a % kRing) * kTileBytes;
+                const uint32_t k1s = base + kOffK + ((a + 1) % kRing) * kTileBytes;
+                const uint32_t p = static_cast<uint32_t>(q0 + 64 + r);
+                const bool q_at_p = r < 64;          // warp-uniform
+                const int qr = q_at_p ? r + 64 : r - 64;
+#pragma unroll 1
+                for (int jj = 0; jj < 4; ++jj) {
+                    // the rows' chunks first (one shared-memory round trip),
+                    // then the angles, then rotate and store
+                    PairChunks vk1, vq, vk0;
+                    pair_load(k1s + r * 128, r, jj, vk1);
+                    pair_load(qs + qr * 128, qr, jj, vq);
+                    if (fresh)
+                        pair_load(k0s + r * 128, r, jj, vk0);
+                    Angles8 an;                       // at p
 #pragma unroll
-                        for (int kx = 0; kx < 32; ++kx)
-                            if (kx < lo || kx > hi)
-                                x[kx] = __float_as_uint(-INFINITY);
+                    for (int i = 0; i < 4; ++i) {
+                        float c0, s0, c1, s1;
+                        pos_cos_sin(p, rope.frac_hi[8 * jj + 2 * i], rope.frac_lo[8 * jj + 2 * i], c0, s0);
+                        pos_cos_sin(p, rope.frac_hi[8 * jj + 2 * i + 1], rope.frac_lo[8 * jj + 2 * i + 1], c1, s1);
+                        an.c[i] = f2(c0, c1);
+                        an.s[i] = f2(s0, s1);
+                        an.ns[i] = f2(-s0, -s1);
                     }
-                };
-                // The reference maximum m (base 2, scaled) is taken from
-                // window chunk 2, which holds the diagonal key i of every
-                // row; p = 2^(s * scale - m) is then written chunk by chunk
-                // in one pass.  Any reference within 2^kSlack of the row
-                // maximum gives the same softmax up to rounding; a chunk
-                // whose maximum exceeds m by more than that raises m and
-                // rescales the P already written (exact powers of two).
-                uint32_t cur[32], nxt[32];
-                tmem_ld32(tm + 32 * wq, cur);
-                tmem_ld32(tm + 32 * (wq + 2), nxt);
-                tmem_wait_ld();
-                reg_fence32(cur);
-                reg_fence32(nxt);
-                mask(nxt, 2);
-                float m = max32(nxt) * kScaleLog2;
-                float sum = 0.f;
-#pragma unroll 1
-                for (int e = 0; e < 5; ++e) {
-                    if (e < 4)
-                        tmem_ld32(tm + 32 * (wq + e + 1), nxt);
-                    mask(cur, e);
-                    const float cmax = max32(cur) * kScaleLog2;
-                    if (__any_sync(0xffffffffu, cmax > m + kSlack)) {
-                        const float mn = fmaxf(m, cmax);
-                        const float f = m == -INFINITY ? 0.f : ex2_approx(m - mn);
-                        tmem_wait_st();
-#pragma unroll 1
-                        for (int e2 = 0; e2 < e; ++e2) {
-                            const int col2 = 32 * (wq + e2);
-                            const uint32_t pa = tm + col2 / 2 + (col2 >= 128 ? 64 : 0);
-                            uint32_t pv[16];
-                            tmem_ld16(pa, pv);
-                            tmem_wait_ld();
+                    pair_rotate_store(k1s + r * 128, r, jj, vk1, an);
+                    if (q_at_p)
+                        pair_rotate_store(qs + qr * 128, qr, jj, vq, an);
+                    if (fresh || !q_at_p) {
+                        // now at p - 128 (one rotation by -128 w):
+                        // c' = c cos + s sin, s' = s cos - c sin
 #pragma unroll
-                            for (int kx = 0; kx < 16; ++kx)
-                                pv[kx] = pack_bf16x2(bf16lo_to_f32(pv[kx]) * f, bf16hi_to_f32(pv[kx]) * f);
-                            tmem_st16(pa, pv);
+                        for (int i = 0; i < 4; ++i) {
+                            const int m = 8 * jj + 2 * i;
+                            const uint64_t c128 = f2(rope.cos128[m], rope.cos128[m + 1]);
+                            const uint64_t s128 = f2(rope.sin128[m], rope.sin128[m + 1]);
+                            const uint64_t c1 = ffma2(an.s[i], s128, fmul2(an.c[i], c128));
+                            const uint64_t s1 = ffma2(an.c[i], f2(-rope.sin128[m], -rope.sin128[m + 1]),
+                                                      fmul2(an.s[i], c128));
+                            an.c[i] = c1;
+                            an.s[i] = s1;
+                            an.ns[i] = fmul2(s1, f2(-1.f, -1.f));
                         }
-                        sum *= f;
-                        m = mn;
-                    }
-                    const float m_use = m == -INFINITY ? 0.f : m;
-                    uint32_t pk[16];
-                    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                    for (int kx = 0; kx < 16; ++kx) {
-                        const float p0 = ex2_approx(fmaf(__uint_as_float(cur[2 * kx]), kScaleLog2, -m_use));
-                        const float p1 = ex2_approx(fmaf(__uint_as_float(cur[2 * kx + 1]), kScaleLog2, -m_use));
-                        a0 += p0;
-                        a1 += p1;
-                        pk[kx] = pack_bf16x2(p0, p1);
-                    }
-                    sum += a0 + a1;
-                    // P chunk of window column c sits at c / 2 (+ 64 in tile
-                    // 1): below every S column not yet read
-                    const int col = 32 * (wq + e);
-                    tmem_st16(tm + col / 2 + (col >= 128 ? 64 : 0), pk);
-                    if (e < 4) {
-                        tmem_wait_ld();
-                        reg_fence32(nxt);
-#pragma unroll
-                        for (int kx = 0; kx < 32; ++kx)
-                            cur[kx] = nxt[kx];
+                        if (!q_at_p)
+                            pair_rotate_store(qs + qr * 128, qr, jj, vq, an);
+                        if (fresh)
+                            pair_rotate_store(k0s + r * 128, r, jj, vk0, an);
                     }
                 }
-                {
-                    uint32_t z[16];
-#pragma unroll
-                    for (int kx = 0; kx < 16; ++kx)
-                        z[kx] = 0u;
-                    for (int c = 0; c < wq; ++c)
-                        tmem_st16(tm + 16 * c, z);
-                    for (int c = wq + 1; c < 4; ++c)
-                        tmem_st16(tm + 128 + 16 * c, z);
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(barp(base, kBarP + g));
-                p_row = i < L ? w.row0 + i : -1;
-                p_col = w.head * kHeadDim;
-                p_inv = sum > 0.f ? 1.f / sum : 0.f;
-                ++j;
+                fence_proxy_async_smem();
             }
-            if (k + 1 < nunits)
-                w.next();
+            mbar_arrive(barp(base, kBarQR + k % kQRing));
+            mbar_arrive(barp(base, kBarKR + (a + 1) % kRing));
+            if (fresh)
+                mbar_arrive(barp(base, kBarKR + a % kRing));
+            if (!ok)
+                break;
+
+            if (j > 0 && !(ok = epilogue(j - 1)))
+                break;
+
+            // ---- softmax of the rows over the window chunks 32q .. 32q + 159
+            const int i = q0 + r;
+            // admitted keys [klo, khi]; none for rows past the sequence
+            const int klo = i < L ? max(0, i - hw) : L, khi = min(L - 1, i + hw);
+            // masked keys of window chunk e -> -inf; only the first and last
+            // chunk, chunks at a sequence edge or a narrower band have any
+            auto mask = [&](uint32_t (&x)[32], int e) {
+                const int key0 = q0 - 64 + 32 * (q + e);
+                if (e == 0 || e == 4 || hw != kBandReach || key0 < 0 || key0 + 31 >= L) {
+                    const int lo = klo - key0, hi = khi - key0;
+#pragma unroll
+                    for (int kx = 0; kx < 32; ++kx)
+                        if (kx < lo || kx > hi)
+                            x[kx] = __float_as_uint(-INFINITY);
+                }
+            };
+            if (!(ok = mbar_wait(barp(base, kBarS + g), static_cast<uint32_t>(j) & 1u, err)))
+                break;
+            __syncwarp();
+            tc_fence_after();
+            // The reference maximum m (base 2, scaled) is taken from window
+            // chunk 2, which holds the diagonal key i of every row; p =
+            // 2^(s * scale - m) is then written chunk by chunk in one pass.
+            // Any reference within 2^kSlack of the row maximum gives the
+            // same softmax up to rounding; a chunk whose maximum exceeds m by
+            // more than that raises m and rescales the P already written
+            // (exact powers of two).
+            uint32_t v[32];
+            tmem_ld32(tm + 32 * (q + 2), v);
+            tmem_wait_ld();
+            reg_fence32(v);
+            mask(v, 2);
+            float m = max32(v) * kScaleLog2;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll 1
+            for (int e = 0; e < 5; ++e) {
+                tmem_ld32(tm + 32 * (q + e), v);
+                tmem_wait_ld();
+                reg_fence32(v);
+                mask(v, e);
+                const float cmax = max32(v) * kScaleLog2;
+                if (__any_sync(0xffffffffu, cmax > m + kSlack)) {
+                    const float mn = fmaxf(m, cmax);
+                    const float f = m == -INFINITY ? 0.f : ex2_approx(m - mn);
+                    tmem_wait_st();
+#pragma unroll 1
+                    for (int e2 = 0; e2 < e; ++e2) {
+                        const int col2 = 32 * (q + e2);
+                        const uint32_t pa = tm + col2 / 2 + (col2 >= 128 ? 64 : 0);
+                        uint32_t pv[16];
+                        tmem_ld16(pa, pv);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int kx = 0; kx < 16; ++kx)
+                            pv[kx] = pack_bf16x2(bf16lo_to_f32(pv[kx]) * f, bf16hi_to_f32(pv[kx]) * f);
+                        tmem_st16(pa, pv);
+                    }
+                    s0 *= f;
+                    s1 *= f;
+                    m = mn;
+                }
+                const float m_use = m == -INFINITY ? 0.f : m;
+                uint32_t pk[16];
+#pragma unroll
+                for (int kx = 0; kx < 16; ++kx) {
+                    float x0 = __uint_as_float(v[2 * kx]), x1 = __uint_as_float(v[2 * kx + 1]);
+                    ffma2_bc(x0, x1, kScaleLog2, -m_use);
+                    x0 = ex2_approx(x0);
+                    x1 = ex2_approx(x1);
+                    fadd2(s0, s1, x0, x1);
+                    pk[kx] = pack_bf16x2(x0, x1);
+                }
+                // P chunk of window column c sits at c / 2 (+ 64 in tile 1):
+                // below every S column not yet read
+                const int col = 32 * (q + e);
+                tmem_st16(tm + col / 2 + (col >= 128 ? 64 : 0), pk);
+            }
+            {
+                uint32_t z[16];
+#pragma unroll
+                for (int kx = 0; kx < 16; ++kx)
+                    z[kx] = 0u;
+                // P = 0 over tile 0's chunks left of the rows' window and
+                // tile 1's chunks right of it
+                for (int c = 0; c < q; ++c)
+                    tmem_st16(tm + 16 * c, z);
+                for (int c = q + 1; c < 4; ++c)
+                    tmem_st16(tm + 128 + 16 * c, z);
+            }
+            p_sum = s0 + s1;
+            if (lead)
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
+                             :: "r"(prev), "r"(row0), "r"(q0), "r"(L), "r"(head) : "memory");
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(barp(base, kBarP + g));
+            ++j;
         }
         if (ok && j > 0)
             epilogue(j - 1);
+        if (lead)
+            bulk_wait0();                               // this group's stores have completed
     }
 
     tc_fence_before();
@@ -666,7 +791,7 @@ cudaError_t launch_attn_local(const LocalArgs &a, cudaStream_t stream)
     if (grid <= 0)
         return cudaSuccess;
     attn_local_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
-        a.tm_qkv, a.rope, a.cu, a.n_seqs, a.T, a.max_seqlen, a.work, a.work_count,
+        a.tm_qkv, a.tm_out, a.rope, a.cu, a.n_seqs, a.T, a.max_seqlen, a.work, a.work_count,
         a.half_window, a.out, a.err);
     return cudaGetLastError();
 }

@@ -429,6 +429,8 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
         LocalArgs la;
         la.rope = h->rope_consts[MBERT_LOCAL];
         la.tm_qkv = a.tm_qkv;
+        if (encode_map(h, &la.tm_out, out, kHidden, T) != MBERT_OK)
+            return MBERT_ERR_CUDA;
         la.cu = cu_seqlens;
         la.n_seqs = n_seqs;
         la.T = T;

@@ -79,6 +79,7 @@ struct RopeConsts {
 struct LocalArgs {
     RopeConsts rope;
     CUtensorMap tm_qkv;          // qkv [T][2304], box 64 x 128, 128B swizzle
+    CUtensorMap tm_out;          // out [T][768], box 64 x 128, 128B swizzle
     const int32_t *cu;
     int n_seqs;
     long long T;
