@@ -50,7 +50,8 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kQRing * kTileBytes;
 constexpr uint32_t kOffV = kOffK + kRing * kTileBytes;
 constexpr uint32_t kOffStage = kOffV + kRing * kTileBytes;   // per group: O tile (bf16) for the TMA store
-constexpr uint32_t kOffRec = kOffStage + 2 * kTileBytes;    // per Q slot: the unit's record (32 bytes)
+constexpr uint32_t kOffBias = kOffStage + 2 * kTileBytes;   // band edge masks: [2 chunks][32 lanes][32] fp32
+constexpr uint32_t kOffRec = kOffBias + 8192;               // per Q slot: the unit's record (32 bytes)
 constexpr uint32_t kOffPrev = kOffRec + kQRing * 32;         // per group: the unit awaiting its epilogue (16 bytes)
 constexpr uint32_t kOffBar = kOffRec + 128;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
@@ -321,6 +322,27 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
     if (warp == 0) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
+    }
+    if (warp == 1) {
+        // The band's edge chunks: in the first window chunk of its rows,
+        // lane l keeps keys k >= l; in the last, k <= l.  As additive masks
+        // (0 keeps, -inf drops), row l of each table, 16-byte chunk c at
+        // c ^ (l % 8).
+        const float ninf = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float b[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int kx = 4 * c + e;
+                    b[e] = (t == 0 ? kx >= lane : kx <= lane) ? 0.f : ninf;
+                }
+                asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};"
+                             :: "r"(base + kOffBias + t * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)),
+                                "f"(b[0]), "f"(b[1]), "f"(b[2]), "f"(b[3]) : "memory");
+            }
     }
     if (tid == 32) {
         tma_prefetch_desc(&tm_qkv);
@@ -663,17 +685,22 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
             const int i = q0 + r;
             // admitted keys [klo, khi]; none for rows past the sequence
             const int klo = i < L ? max(0, i - hw) : L, khi = min(L - 1, i + hw);
-            // masked keys of window chunk e -> -inf; only the first and last
-            // chunk, chunks at a sequence edge or a narrower band have any
-            auto mask = [&](uint32_t (&x)[32], int e) {
+            // Keys outside [klo, khi] of window chunk e -> -inf, from a bit
+            // mask of the admitted keys; needed only where a chunk meets a
+            // sequence edge or the band is narrower.  The band's own edge
+            // chunks (e = 0 and 4) take their masks from the lane tables.
+            auto general = [&](int e) {
                 const int key0 = q0 - 64 + 32 * (q + e);
-                if (e == 0 || e == 4 || hw != kBandReach || key0 < 0 || key0 + 31 >= L) {
-                    const int lo = klo - key0, hi = khi - key0;
+                return hw != kBandReach || key0 < 0 || key0 + 31 >= L;
+            };
+            auto mask_bits = [&](uint32_t (&x)[32], int e) {
+                const int key0 = q0 - 64 + 32 * (q + e);
+                const int lo = klo - key0, hi = khi - key0;
+                const uint32_t keep = (lo > 31 || hi < 0 || lo > hi) ? 0u
+                    : ((0xFFFFFFFFu >> (31 - min(hi, 31))) & (0xFFFFFFFFu << max(lo, 0)));
 #pragma unroll
-                    for (int kx = 0; kx < 32; ++kx)
-                        if (kx < lo || kx > hi)
-                            x[kx] = __float_as_uint(-INFINITY);
-                }
+                for (int kx = 0; kx < 32; ++kx)
+                    x[kx] = (keep & (1u << kx)) ? x[kx] : __float_as_uint(-INFINITY);
             };
             if (!(ok = mbar_wait(barp(base, kBarS + g), static_cast<uint32_t>(j) & 1u, err)))
                 break;
@@ -683,14 +710,15 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
             // chunk 2, which holds the diagonal key i of every row; p =
             // 2^(s * scale - m) is then written chunk by chunk in one pass.
             // Any reference within 2^kSlack of the row maximum gives the
-            // same softmax up to rounding; a chunk whose maximum exceeds m by
-            // more than that raises m and rescales the P already written
-            // (exact powers of two).
+            // same softmax up to rounding; a chunk whose exponents exceed
+            // kSlack raises m and rescales the P already written (exact
+            // powers of two).
             uint32_t v[32];
             tmem_ld32(tm + 32 * (q + 2), v);
             tmem_wait_ld();
             reg_fence32(v);
-            mask(v, 2);
+            if (general(2))
+                mask_bits(v, 2);
             float m = max32(v) * kScaleLog2;
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll 1
@@ -698,11 +726,52 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
                 tmem_ld32(tm + 32 * (q + e), v);
                 tmem_wait_ld();
                 reg_fence32(v);
-                mask(v, e);
-                const float cmax = max32(v) * kScaleLog2;
-                if (__any_sync(0xffffffffu, cmax > m + kSlack)) {
-                    const float mn = fmaxf(m, cmax);
-                    const float f = m == -INFINITY ? 0.f : ex2_approx(m - mn);
+                const float m_use = m == -INFINITY ? 0.f : m;
+                // exponents y = s * scale - m (+ the lane's edge mask)
+                if (general(e)) {
+                    mask_bits(v, e);
+#pragma unroll
+                    for (int kx = 0; kx < 16; ++kx) {
+                        float x0 = __uint_as_float(v[2 * kx]), x1 = __uint_as_float(v[2 * kx + 1]);
+                        ffma2_bc(x0, x1, kScaleLog2, -m_use);
+                        v[2 * kx] = __float_as_uint(x0);
+                        v[2 * kx + 1] = __float_as_uint(x1);
+                    }
+                } else if (e == 0 || e == 4) {
+                    const uint32_t tab = base + kOffBias + (e == 4 ? 4096 : 0) + lane * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float b[4];
+                        asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                                     : "=f"(b[0]), "=f"(b[1]), "=f"(b[2]), "=f"(b[3])
+                                     : "r"(tab + ((c ^ (lane & 7)) << 4)));
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const uint64_t y = ffma2(f2(__uint_as_float(v[4 * c + 2 * t]), __uint_as_float(v[4 * c + 2 * t + 1])),
+                                                     f2(kScaleLog2, kScaleLog2),
+                                                     f2(b[2 * t] - m_use, b[2 * t + 1] - m_use));
+                            float y0, y1;
+                            f2_split(y, y0, y1);
+                            v[4 * c + 2 * t] = __float_as_uint(y0);
+                            v[4 * c + 2 * t + 1] = __float_as_uint(y1);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int kx = 0; kx < 16; ++kx) {
+                        float x0 = __uint_as_float(v[2 * kx]), x1 = __uint_as_float(v[2 * kx + 1]);
+                        ffma2_bc(x0, x1, kScaleLog2, -m_use);
+                        v[2 * kx] = __float_as_uint(x0);
+                        v[2 * kx + 1] = __float_as_uint(x1);
+                    }
+                }
+                const float ymax = max32(v);
+                if (__any_sync(0xffffffffu, ymax > kSlack)) {
+                    // raise m by d (0 in lanes that need no change) and
+                    // rescale this chunk's exponents, the P already written
+                    // and the sums by 2^-d
+                    const float d = ymax > kSlack ? ymax : 0.f;
+                    const float f = ex2_approx(-d);
                     tmem_wait_st();
 #pragma unroll 1
                     for (int e2 = 0; e2 < e; ++e2) {
@@ -716,20 +785,20 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
                             pv[kx] = pack_bf16x2(bf16lo_to_f32(pv[kx]) * f, bf16hi_to_f32(pv[kx]) * f);
                         tmem_st16(pa, pv);
                     }
+#pragma unroll
+                    for (int kx = 0; kx < 32; ++kx)
+                        v[kx] = __float_as_uint(__uint_as_float(v[kx]) - d);
                     s0 *= f;
                     s1 *= f;
-                    m = mn;
+                    m = m_use + d;
                 }
-                const float m_use = m == -INFINITY ? 0.f : m;
                 uint32_t pk[16];
 #pragma unroll
                 for (int kx = 0; kx < 16; ++kx) {
-                    float x0 = __uint_as_float(v[2 * kx]), x1 = __uint_as_float(v[2 * kx + 1]);
-                    ffma2_bc(x0, x1, kScaleLog2, -m_use);
-                    x0 = ex2_approx(x0);
-                    x1 = ex2_approx(x1);
-                    fadd2(s0, s1, x0, x1);
-                    pk[kx] = pack_bf16x2(x0, x1);
+                    const float p0 = ex2_approx(__uint_as_float(v[2 * kx]));
+                    const float p1 = ex2_approx(__uint_as_float(v[2 * kx + 1]));
+                    fadd2(s0, s1, p0, p1);
+                    pk[kx] = pack_bf16x2(p0, p1);
                 }
                 // P chunk of window column c sits at c / 2 (+ 64 in tile 1):
                 // below every S column not yet read
