@@ -43,6 +43,17 @@ BYTES_PER_TOKEN = (2304 + 768) * 2             # read qkv once, write out once
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 N_SETS = 6
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# the ncu captures of the one-sequence 8192-token workload summarised in
+# profiles/attn_{global,local}_kernel_config3.md.  Reported only while the
+# kernel sources still hash to what was captured.
+NCU_TRAFFIC = {
+    "global": {"bytes": 39.98e6, "kernel": "attn_global_kernel",
+               "sources": {"attn_global.cu": "89c3d2ad0d680903", "common.cuh": "42f2174ca3b5eb40"}},
+    "local": {"bytes": 37.85e6, "kernel": "attn_local_kernel",
+              "sources": {"attn_local.cu": "0bc14693bd260833", "common.cuh": "42f2174ca3b5eb40"}},
+}
+
 WORKLOADS = {
     "config3": (3, "1 sequence x 8192 tokens, qkv [8192,2304] bf16 ~ N(0,1), seed 3"),
     "config4": (4, "65536 tokens, L ~ U{128..8192} packed, qkv bf16 ~ N(0,0.5), seed 4"),
@@ -81,6 +92,24 @@ def load_peaks():
         return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
     except (OSError, KeyError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def captured_traffic(kind, workload):
+    """DRAM bytes per launch of the layer's attention kernel, or None if the
+    capture does not apply (another workload, or the kernel source changed)."""
+    import hashlib
+    rec = NCU_TRAFFIC[kind]
+    if workload != "config3":
+        return None
+    csrc = os.path.join(ROOT, "encoder_only_transformer_gb300", "csrc")
+    for name, digest in rec["sources"].items():
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest()[:16] != digest:
+                    return None
+        except OSError:
+            return None
+    return rec["bytes"]
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -313,11 +342,21 @@ def run_ours(args):
             "gflop": wk["flops"] / 1e9,
             "mbytes": wk["bytes"] / 1e6,
         }
-    g = layers["global"]
+    g, lo = layers["global"], layers["local"]
+    # The dominant kernel (the global layer's) against the tensor peak; the
+    # local layer's kernel, HBM bound, against the copy bandwidth.  Kernel
+    # times are CUDA-event pairs around each launch over the timed region,
+    # with the SM clock at its maximum (see "clocks"), so the burst peaks.
     roofline = {"bound": "tensor", "achieved": g["tflops"], "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": g["tflops"] / peaks["bf16_tflops"], "traffic": None,
-                "kernel": "attn_generic_kernel (global layer)",
+                "unit": "TFLOP/s", "frac": g["tflops"] / peaks["bf16_tflops"],
+                "traffic": captured_traffic("global", args.workload),
+                "kernel": "attn_global_kernel (global layer)",
                 "peak_source": f"{src} bf16_tflops (burst)"}
+    roofline_local = {"bound": "hbm", "achieved": lo["hbm_gbs"], "peak": peaks["hbm_gbs"],
+                      "unit": "GB/s", "frac": lo["hbm_gbs"] / peaks["hbm_gbs"],
+                      "traffic": captured_traffic("local", args.workload),
+                      "kernel": "attn_local_kernel (local layer)",
+                      "peak_source": f"{src} hbm_gbs"}
     rec = {
         "metric": METRIC,
         "value": whole_job_tokens_per_s(T, world, ms_step),
@@ -337,6 +376,7 @@ def run_ours(args):
                    "parallelism": f"{world} independent replica(s), no collective"},
         "layers": layers,
         "roofline": roofline,
+        "roofline_local": roofline_local,
         "gpu_launches": launches,
         "clocks": clock_rec,
         "e2e": {"value": whole_job_tokens_per_s(T, world, e2e_ms), "unit": UNIT,
