@@ -225,7 +225,9 @@ struct Walker {
     int row0, L;
     bool fresh;
 
-    __device__ void start(const int32_t *cu_, const int2 *work_, int G_, long long u, int seq0, int qb0)
+    // First unit u; without a work list its sequence, block, first row and
+    // length are given (found by the range search).
+    __device__ void start(const int32_t *cu_, const int2 *work_, int G_, long long u, const int (&first)[4])
     {
         cu = cu_;
         work = work_;
@@ -236,12 +238,14 @@ struct Walker {
             const int2 w = work[e];
             seq = w.x;
             qb = w.y;
+            row0 = cu[seq];
+            L = cu[seq + 1] - row0;
         } else {
-            seq = seq0;
-            qb = qb0;
+            seq = first[0];
+            qb = first[1];
+            row0 = first[2];
+            L = first[3];
         }
-        row0 = cu[seq];
-        L = cu[seq + 1] - row0;
         fresh = true;
     }
 
@@ -286,44 +290,96 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ long long s_range[2];
-    __shared__ int s_first[3];
+    __shared__ int s_g;
+    __shared__ int s_first[4];       // first unit: sequence, block, first row, length
     __shared__ uint32_t s_tmem;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // ---- this CTA's range of units [u_lo, u_hi) of heads x G
+    // ---- setup, in parallel: warp 0 finds this CTA's range [u_lo, u_hi) of
+    // the heads x G units; warp 1 allocates TMEM and writes the band mask
+    // tables; warp 2 initialises the barriers.
     if (warp == 0) {
-        int G = work ? *work_count : count_blocks(cu, n_seqs, T, max_seqlen, err);
+        int G = 0, seq0 = 0, qb0 = 0, row00 = 0, L0 = 0;
         long long lo = 0, hi = 0;
-        if (G > 0) {
+        if (work) {
+            G = *work_count;
+        } else if (n_seqs <= 32) {
+            // one sequence per lane: check, count and locate in one pass
+            int c0 = 0, c1 = 0;
+            if (lane < n_seqs) {
+                c0 = cu[lane];
+                c1 = cu[lane + 1];
+            }
+            const int Ls = c1 - c0;
+            int bad = 0;
+            if (lane < n_seqs) {
+                if (Ls < 0)
+                    bad |= kErrBadCu;
+                else if (Ls > max_seqlen)
+                    bad |= kErrTooLong;
+            }
+            if ((lane == 0 && c0 != 0) || (lane == n_seqs - 1 && static_cast<long long>(c1) != T))
+                bad |= kErrBadCu;
+            const int nb = (lane < n_seqs && Ls > 0) ? (Ls + kBlockM - 1) / kBlockM : 0;
+            int incl = nb;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d)
+                    incl += v;
+            }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1)
+                bad |= __shfl_xor_sync(0xffffffffu, bad, d);
+            G = __shfl_sync(0xffffffffu, incl, 31);
+            if (bad) {
+                if (blockIdx.x == 0 && lane == 0)
+                    atomicOr(err, bad);
+                G = -1;
+            } else if (G > 0) {
+                const long long U = static_cast<long long>(kHeads) * G;
+                lo = U * blockIdx.x / gridDim.x;
+                hi = U * (blockIdx.x + 1) / gridDim.x;
+                const int e0 = static_cast<int>(lo % G), excl = incl - nb;
+                const unsigned hit = __ballot_sync(0xffffffffu, nb > 0 && e0 >= excl && e0 < excl + nb);
+                const int src = hit ? __ffs(hit) - 1 : 0;
+                seq0 = src;
+                qb0 = e0 - __shfl_sync(0xffffffffu, excl, src);
+                row00 = __shfl_sync(0xffffffffu, c0, src);
+                L0 = __shfl_sync(0xffffffffu, Ls, src);
+            }
+        } else {
+            G = count_blocks(cu, n_seqs, T, max_seqlen, err);
+            if (G > 0) {
+                const long long U = static_cast<long long>(kHeads) * G;
+                lo = U * blockIdx.x / gridDim.x;
+                hi = U * (blockIdx.x + 1) / gridDim.x;
+                if (lo < hi) {
+                    locate_block(cu, n_seqs, static_cast<int>(lo % G), seq0, qb0);
+                    row00 = cu[seq0];
+                    L0 = cu[seq0 + 1] - row00;
+                }
+            }
+        }
+        if (work && G > 0) {
             const long long U = static_cast<long long>(kHeads) * G;
             lo = U * blockIdx.x / gridDim.x;
             hi = U * (blockIdx.x + 1) / gridDim.x;
         }
-        int seq0 = 0, qb0 = 0;
-        if (lo < hi && !work)
-            locate_block(cu, n_seqs, static_cast<int>(lo % G), seq0, qb0);
         if (lane == 0) {
             s_range[0] = lo;
             s_range[1] = hi;
-            s_first[0] = G;
-            s_first[1] = seq0;
-            s_first[2] = qb0;
+            s_g = G;
+            s_first[0] = seq0;
+            s_first[1] = qb0;
+            s_first[2] = row00;
+            s_first[3] = L0;
         }
-    }
-    __syncthreads();
-    const long long u_lo = s_range[0];
-    const int nunits = static_cast<int>(s_range[1] - u_lo);
-    if (nunits <= 0)
-        return;
-    const int G = s_first[0];
-
-    if (warp == 0) {
+    } else if (warp == 1) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
-    }
-    if (warp == 1) {
         // The band's edge chunks: in the first window chunk of its rows,
         // lane l keeps keys k >= l; in the last, k <= l.  As additive masks
         // (0 keeps, -inf drops), row l of each table, 16-byte chunk c at
@@ -343,8 +399,7 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
                              :: "r"(base + kOffBias + t * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)),
                                 "f"(b[0]), "f"(b[1]), "f"(b[2]), "f"(b[3]) : "memory");
             }
-    }
-    if (tid == 32) {
+    } else if (tid == 64) {
         tma_prefetch_desc(&tm_qkv);
         tma_prefetch_desc(&tm_out);
         for (int i = 0; i < kNumBars; ++i) {
@@ -361,13 +416,25 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const long long u_lo = s_range[0];
+    const int nunits = static_cast<int>(s_range[1] - u_lo);
+    if (nunits <= 0) {
+        if (warp == 1)
+            tmem_dealloc(s_tmem, kTmemCols);
+        return;
+    }
+    const int G = s_g;
+    int first[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        first[i] = s_first[i];
     const uint32_t tmem = s_tmem;
 
     if (warp >= kWarpProducer) {
         if (warp == kWarpProducer) {
             // ------------------------------------------------------ producer
             Walker w;
-            w.start(cu, work, G, u_lo, s_first[1], s_first[2]);
+            w.start(cu, work, G, u_lo, first);
             const uint64_t once = l2_policy_evict_first();
             int nq = 0, tk = 0, tv = 0;   // tiles issued per ring (issued in index order)
             bool ok = true;
@@ -445,7 +512,7 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
         } else if (warp == kWarpMma || warp == kWarpMma + 1) {
             // ------------------------------------------------------ MMA issuers
             Walker w;
-            w.start(cu, work, G, u_lo, s_first[1], s_first[2]);
+            w.start(cu, work, G, u_lo, first);
             const int g = warp - kWarpMma;
             const uint32_t tm = tmem + g * kGroupCols;
             bool ok = true;
@@ -834,7 +901,7 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
