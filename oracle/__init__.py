@@ -53,6 +53,9 @@ def lib():
                                        ctypes.c_int, ctypes.c_double, ctypes.c_int, i64p,
                                        ctypes.c_int64, dp, i32p, ctypes.c_int]
         L.oracle_attention.restype = ctypes.c_int
+        L.oracle_out_proj.argtypes = [u16p, u16p, u16p, ctypes.c_int64, ctypes.c_int, i64p,
+                                      ctypes.c_int64, dp, ctypes.c_int]
+        L.oracle_out_proj.restype = ctypes.c_int
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = ctypes.c_int
         _lib = L
@@ -148,6 +151,34 @@ def attention(qkv_bits, cu_seqlens, theta: float, half_window: int, rows=None,
     if rc:
         raise ValueError(f"oracle_attention failed (code {rc})")
     return out, counts
+
+
+def out_proj(a_bits, wo_bits, x_bits, rows=None, threads: int = 0):
+    """y = x + a Wo^T in fp64 (Wo stored [out][in]).
+
+    a_bits, x_bits: uint16 [T, d] bf16 bit patterns (joined head outputs and
+    the residual stream); wo_bits: uint16 [d, d].  rows: None (every row) or
+    sorted packed row indices.  Returns fp64 [n, d].
+    """
+    a = np.ascontiguousarray(a_bits)
+    x = np.ascontiguousarray(x_bits)
+    w = np.ascontiguousarray(wo_bits)
+    if a.dtype != np.uint16 or x.dtype != np.uint16 or w.dtype != np.uint16:
+        raise TypeError("inputs must be uint16 bf16 bit patterns")
+    T, d = a.shape
+    assert x.shape == (T, d) and w.shape == (d, d)
+    if rows is None:
+        n, rp = T, None
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        n, rp = r.shape[0], _ptr(r, ctypes.c_int64)
+    y = np.empty((n, d), dtype=np.float64)
+    rc = lib().oracle_out_proj(_ptr(a, ctypes.c_uint16), _ptr(w, ctypes.c_uint16),
+                               _ptr(x, ctypes.c_uint16), T, d, rp, n,
+                               _ptr(y, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError(f"oracle_out_proj failed (code {rc})")
+    return y
 
 
 def attention_kind(qkv_bits, cu_seqlens, kind: str, rows=None, threads: int = 0):

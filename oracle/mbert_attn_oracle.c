@@ -431,6 +431,59 @@ int oracle_attention(const uint16_t *qkv, int64_t T, int heads, int head_dim,
     return failed ? -20 : 0;
 }
 
+int oracle_max_threads(void);
+
+/* ------------------------------------------------------------------ */
+/* output projection and residual add                                  */
+/* ------------------------------------------------------------------ */
+
+/* y[t][o] = x[t][o] + sum_c a[t][c] * wo[o][c] over c = 0 .. d - 1: the
+ * joined head outputs a (bf16 [T][d]) mapped back to the model width by Wo,
+ * stored [out][in] ("ModernBERT-base Architecture Teardown", "How Does
+ * ModernBERT Make Q, K and V?": Wo maps the joined heads from 768 back to
+ * 768, a Linear weight stored [out, in]), and added to the residual stream
+ * x (bf16 [T][d]; "ModernBertModel", "Implementing it": x = x + a Wo^T).
+ * Every product and sum in fp64; y is fp64 [T][d].  rows: NULL (every row)
+ * or n sorted row indices, y then [n][d]. */
+int oracle_out_proj(const uint16_t *a, const uint16_t *wo, const uint16_t *x, int64_t T, int d,
+                    const int64_t *rows, int64_t n, double *y, int threads)
+{
+    if (T < 0 || d <= 0 || n < 0)
+        return -1;
+    if (!rows)
+        n = T;
+    double *w = malloc(sizeof(double) * (size_t)d * (size_t)d);
+    if (!w)
+        return -2;
+    for (int64_t e = 0; e < (int64_t)d * d; e++)
+        w[e] = bf16_to_f64(wo[e]);
+    int bad = 0;
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : oracle_max_threads()) reduction(|:bad)
+    for (int64_t k = 0; k < n; k++) {
+        const int64_t t = rows ? rows[k] : k;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        double *ar = malloc(sizeof(double) * (size_t)d);
+        if (!ar) {
+            bad = 1;
+            continue;
+        }
+        for (int c = 0; c < d; c++)
+            ar[c] = bf16_to_f64(a[t * d + c]);
+        for (int o = 0; o < d; o++) {
+            double acc = 0.0;
+            for (int c = 0; c < d; c++)
+                acc += ar[c] * w[(int64_t)o * d + c];
+            y[k * d + o] = bf16_to_f64(x[t * d + o]) + acc;
+        }
+        free(ar);
+    }
+    free(w);
+    return bad ? -3 : 0;
+}
+
 /* Number of OpenMP threads a parallel region would use by default. */
 int oracle_max_threads(void)
 {

@@ -14,6 +14,7 @@ import pytest
 import oracle
 from oracle import build as obuild
 import test_oracle as T
+import test_oracle_out_proj as P
 
 # (name, original source fragment, planted fragment)
 PLANTS = [
@@ -29,6 +30,10 @@ PLANTS = [
     ("softmax_without_max", "den += exp(scores[j] - m);", "den += exp(scores[j]);"),
     ("freq_exponent", "inv_freq[m] = pow(theta, -2.0 * (double)m / (double)head_dim);",
      "inv_freq[m] = pow(theta, -1.0 * (double)m / (double)head_dim);"),
+    ("out_proj_transposed", "acc += ar[c] * w[(int64_t)o * d + c];",
+     "acc += ar[c] * w[(int64_t)c * d + o];"),
+    ("out_proj_without_residual", "y[k * d + o] = bf16_to_f64(x[t * d + o]) + acc;",
+     "y[k * d + o] = acc;"),
 ]
 
 
@@ -47,6 +52,8 @@ def _pins():
         T.test_length_one_sequence_returns_its_value,
         T.test_unit_values_give_unit_outputs,
     ]
+    out += [P.test_hand_worked_example, P.test_permutation_weight_permutes_columns,
+            P.test_zero_weight_returns_the_residual, P.test_power_of_two_diagonal]
     out += [(lambda r=r: T.test_key_counts_match_pages(r)) for r in table]
     for lengths in ([5, 64, 65], [130, 7, 200]):
         for kind in ("global", "local"):
