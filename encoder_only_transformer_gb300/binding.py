@@ -37,6 +37,7 @@ SIGNATURES = {
     "mbert_attn_reserve": (_c_int, [_vp, _c_i64, _c_i64]),
     "mbert_attn_forward": (_c_int, [_vp, _vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp]),
     "mbert_attn_key_counts": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp]),
+    "mbert_attn_out_proj": (_c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _vp]),
     "mbert_attn_get_error": (_c_int, [_vp]),
     "mbert_attn_selftest_timeout": (_c_int, [_vp, _c_i64, _vp]),
     "mbert_attn_forward_noalloc": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp,
@@ -177,6 +178,26 @@ class Attention:
         _check(st, "forward")
         return out
 
+    def out_proj(self, a: torch.Tensor, wo: torch.Tensor, x: torch.Tensor,
+                 out: torch.Tensor = None) -> torch.Tensor:
+        """y[T, 768] bf16 = x + a Wo^T: the output projection (Wo [768, 768],
+        stored [out, in]) with the residual add.  `out` may be `x` itself."""
+        def check(t, name, shape):
+            if (t.dtype != torch.bfloat16 or tuple(t.shape) != shape or t.device != self.device
+                    or not t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous bf16 {list(shape)} tensor on {self.device}")
+        T = a.shape[0] if a.dim() == 2 else -1
+        check(a, "a", (T, OUT_WIDTH))
+        check(wo, "wo", (OUT_WIDTH, OUT_WIDTH))
+        check(x, "x", (T, OUT_WIDTH))
+        if out is None:
+            out = torch.empty(T, OUT_WIDTH, dtype=torch.bfloat16, device=self.device)
+        check(out, "out", (T, OUT_WIDTH))
+        st = load_library().mbert_attn_out_proj(self._h, a.data_ptr(), wo.data_ptr(), x.data_ptr(),
+                                                T, out.data_ptr(), _stream_ptr(self.device))
+        _check(st, "out_proj")
+        return out
+
     def key_counts(self, cu_seqlens: torch.Tensor, total_tokens: int, layer_kind,
                    max_seqlen: int = 0) -> torch.Tensor:
         """int32 [T]: keys the kernels' schedule and mask admit per query row."""
@@ -196,18 +217,19 @@ class Attention:
                "selftest_timeout")
 
     def profile(self, enable: bool = True):
-        """Record a CUDA event pair around every attention kernel."""
+        """Record a CUDA event pair around every attention and projection kernel."""
         _check(load_library().mbert_attn_profile_enable(self._h, 1 if enable else 0), "profile")
 
     def profile_read(self):
-        """-> ({'global': ms, 'local': ms}, {'global': n, 'local': n}, total_launches);
-        synchronises and clears the record."""
-        ms = (ctypes.c_double * 2)()
-        n = (ctypes.c_int64 * 2)()
+        """-> ({'global': ms, 'local': ms, 'out_proj': ms}, the same keys -> kernel
+        count, total_launches); synchronises and clears the record."""
+        ms = (ctypes.c_double * 3)()
+        n = (ctypes.c_int64 * 3)()
         tot = ctypes.c_int64()
         _check(load_library().mbert_attn_profile_read(self._h, ms, n, ctypes.byref(tot)),
                "profile_read")
-        return ({"global": ms[0], "local": ms[1]}, {"global": n[0], "local": n[1]},
+        keys = ("global", "local", "out_proj")
+        return ({k: ms[i] for i, k in enumerate(keys)}, {k: n[i] for i, k in enumerate(keys)},
                 int(tot.value))
 
     def get_error(self) -> int:
@@ -234,6 +256,13 @@ def attention(qkv: torch.Tensor, cu_seqlens: torch.Tensor, layer_kind, max_seqle
     if not qkv.is_cuda:
         raise ValueError("qkv must be a CUDA tensor")
     return _default(qkv.device).forward(qkv, cu_seqlens, layer_kind, max_seqlen, out)
+
+
+def out_proj(a: torch.Tensor, wo: torch.Tensor, x: torch.Tensor, out: torch.Tensor = None) -> torch.Tensor:
+    """y = x + a Wo^T (bf16, CUDA tensors): the step after the attention block."""
+    if not a.is_cuda:
+        raise ValueError("a must be a CUDA tensor")
+    return _default(a.device).out_proj(a, wo, x, out=out)
 
 
 def key_counts(cu_seqlens: torch.Tensor, total_tokens: int, layer_kind) -> torch.Tensor:

@@ -29,6 +29,7 @@ constexpr int kTileBytes = kBlockM * kHeadDim * 2;  // 16 KB bf16 tile
 constexpr int kErrBadCu = 1;
 constexpr int kErrTooLong = 2;
 constexpr int kErrTimeout = 4;
+constexpr int kErrPairTmem = 8;   // a CTA pair's TMEM allocations disagree
 
 // bounded waits give up after this long (ns) and report kErrTimeout
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -128,6 +129,22 @@ __device__ __forceinline__ uint32_t elect_one_sync()
     return pred;
 }
 
+// ---- thread-block clusters ----
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA in the cluster arrives (release) and waits
+// (acquire).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\t"
+                 "barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // ---- mbarrier ----
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
@@ -224,6 +241,14 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar),
            "l"(policy)
         : "memory");
+}
+
+// Fetch `bytes` (a multiple of 16) from a 16-byte aligned global address
+// into L2, with no completion to wait for.
+__device__ __forceinline__ void l2_prefetch_bytes(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 :: "l"(reinterpret_cast<uint64_t>(p)), "r"(bytes) : "memory");
 }
 
 // 2-D tiled store of the box at (x = column, y = row) from shared memory

@@ -43,9 +43,21 @@ struct mbert_attn {
     EncodeTiledFn encode = nullptr;
     // measurement: event pairs around the attention kernel, per layer kind
     bool profiling = false;
-    std::vector<cudaEvent_t> ev[2];         // start, end, start, end, ...
-    size_t ev_used[2] = {0, 0};
+    // start, end, start, end, ... per profile slot (global, local, projection)
+    std::vector<cudaEvent_t> ev[MBERT_PROFILE_SLOTS];
+    size_t ev_used[MBERT_PROFILE_SLOTS] = {};
     int64_t launches = 0;                   // every kernel this handle enqueued
+    // recently encoded tensor maps, by (address, width, rows): encoding one
+    // costs microseconds of host time, as much as a short kernel
+    struct MapEntry {
+        const void *ptr = nullptr;
+        int width = 0;
+        int64_t rows = -1;
+        uint64_t used = 0;
+        CUtensorMap map;
+    };
+    MapEntry maps[32];
+    uint64_t map_clock = 0;
 };
 
 namespace {
@@ -141,8 +153,37 @@ int grow_workspace(mbert_attn *h, int64_t entries, int64_t rot_rows)
 
 // 2-D bf16 tensor map over [rows][width] (row pitch = width * 2 bytes),
 // box 64 columns x 128 rows, 128-byte swizzle, out-of-range reads give 0.
+// The next event pair of a profile slot (both null while profiling is off).
+int profile_events(mbert_attn *h, int slot, cudaEvent_t *ev0, cudaEvent_t *ev1)
+{
+    *ev0 = *ev1 = nullptr;
+    if (!h->profiling)
+        return MBERT_OK;
+    std::vector<cudaEvent_t> &v = h->ev[slot];
+    while (v.size() < h->ev_used[slot] + 2) {
+        cudaEvent_t x;
+        if (cudaEventCreate(&x) != cudaSuccess)
+            return MBERT_ERR_CUDA;
+        v.push_back(x);
+    }
+    *ev0 = v[h->ev_used[slot]];
+    *ev1 = v[h->ev_used[slot] + 1];
+    h->ev_used[slot] += 2;
+    return MBERT_OK;
+}
+
 int encode_map(mbert_attn *h, CUtensorMap *tm, const void *ptr, int width, int64_t rows)
 {
+    mbert_attn::MapEntry *victim = &h->maps[0];
+    for (auto &m : h->maps) {
+        if (m.ptr == ptr && m.width == width && m.rows == rows) {
+            m.used = ++h->map_clock;
+            *tm = m.map;
+            return MBERT_OK;
+        }
+        if (m.used < victim->used)
+            victim = &m;
+    }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(width) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(kBlockM)};
@@ -151,7 +192,14 @@ int encode_map(mbert_attn *h, CUtensorMap *tm, const void *ptr, int width, int64
                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? MBERT_OK : MBERT_ERR_CUDA;
+    if (r != CUDA_SUCCESS)
+        return MBERT_ERR_CUDA;
+    victim->ptr = ptr;
+    victim->width = width;
+    victim->rows = rows;
+    victim->used = ++h->map_clock;
+    victim->map = *tm;
+    return MBERT_OK;
 }
 
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb)
@@ -227,7 +275,7 @@ MBERT_API void mbert_attn_destroy(mbert_attn *h)
         return;
     {
         DeviceGuard g(h->device);
-        for (int k = 0; k < 2; ++k)
+        for (int k = 0; k < MBERT_PROFILE_SLOTS; ++k)
             for (cudaEvent_t e : h->ev[k])
                 cudaEventDestroy(e);
         cudaFree(h->rope[0]);
@@ -410,18 +458,8 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
     a.partials = h->partials;
 
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
-    if (h->profiling) {
-        std::vector<cudaEvent_t> &v = h->ev[layer_kind];
-        while (v.size() < h->ev_used[layer_kind] + 2) {
-            cudaEvent_t x;
-            if (cudaEventCreate(&x) != cudaSuccess)
-                return MBERT_ERR_CUDA;
-            v.push_back(x);
-        }
-        ev0 = v[h->ev_used[layer_kind]];
-        ev1 = v[h->ev_used[layer_kind] + 1];
-        h->ev_used[layer_kind] += 2;
-    }
+    if (profile_events(h, layer_kind, &ev0, &ev1) != MBERT_OK)
+        return MBERT_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (layer_kind == MBERT_LOCAL && h->cfg.half_window <= kBandReach) {
         // RoPE inside the attention kernel; with few sequences each CTA finds
@@ -498,6 +536,49 @@ MBERT_API int mbert_attn_key_counts(mbert_attn *h, const int32_t *cu_seqlens, in
     return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
 }
 
+MBERT_API int mbert_attn_out_proj(mbert_attn *h, const void *a, const void *wo, const void *x,
+                                  int64_t total_tokens, void *y, void *stream)
+{
+    if (!h || total_tokens < 0 || total_tokens > INT32_MAX)
+        return MBERT_ERR_BAD_ARG;
+    const int64_t T = total_tokens;
+    if (T == 0)
+        return MBERT_OK;
+    if (!a || !wo || !x || !y)
+        return MBERT_ERR_BAD_ARG;
+    for (const void *ptr : {a, wo, x, static_cast<const void *>(y)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15)
+            return MBERT_ERR_BAD_ARG;
+    const size_t act = static_cast<size_t>(T) * kHidden * 2;
+    const size_t wbytes = static_cast<size_t>(kHidden) * kHidden * 2;
+    if (ranges_overlap(a, act, y, act) || ranges_overlap(wo, wbytes, y, act) ||
+        (x != y && ranges_overlap(x, act, y, act)))
+        return MBERT_ERR_BAD_ARG;
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    OutProjArgs o;
+    if (encode_map(h, &o.tm_a, a, kHidden, T) != MBERT_OK ||
+        encode_map(h, &o.tm_w, wo, kHidden, kHidden) != MBERT_OK ||
+        encode_map(h, &o.tm_x, x, kHidden, T) != MBERT_OK ||
+        encode_map(h, &o.tm_y, y, kHidden, T) != MBERT_OK)
+        return MBERT_ERR_CUDA;
+    o.x = static_cast<const __nv_bfloat16 *>(x);
+    o.T = T;
+    o.num_ctas = h->num_sms;
+    o.err = h->err;
+    cudaEvent_t ev0, ev1;
+    if (profile_events(h, MBERT_PROFILE_OUT_PROJ, &ev0, &ev1) != MBERT_OK)
+        return MBERT_ERR_CUDA;
+    cudaError_t e = ev0 ? cudaEventRecord(ev0, st) : cudaSuccess;
+    if (e == cudaSuccess)
+        e = launch_out_proj(o, st);
+    if (e == cudaSuccess && ev1)
+        e = cudaEventRecord(ev1, st);
+    h->launches += 1;
+    h->last_stream = st;
+    return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
+}
+
 MBERT_API int mbert_attn_get_error(mbert_attn *h)
 {
     if (!h)
@@ -511,6 +592,8 @@ MBERT_API int mbert_attn_get_error(mbert_attn *h)
         return MBERT_ERR_CUDA;
     if (word & kErrTimeout)
         return MBERT_ERR_TIMEOUT;
+    if (word & kErrPairTmem)
+        return MBERT_ERR_CUDA;
     if (word & kErrBadCu)
         return MBERT_ERR_BAD_CU_SEQLENS;
     if (word & kErrTooLong)
@@ -538,13 +621,13 @@ MBERT_API int mbert_attn_profile_enable(mbert_attn *h, int enable)
     return MBERT_OK;
 }
 
-MBERT_API int mbert_attn_profile_read(mbert_attn *h, double *attn_ms, int64_t *attn_launches,
+MBERT_API int mbert_attn_profile_read(mbert_attn *h, double *kernel_ms, int64_t *kernel_launches,
                                       int64_t *total_launches)
 {
     if (!h)
         return MBERT_ERR_BAD_ARG;
     DeviceGuard g(h->device);
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < MBERT_PROFILE_SLOTS; ++k) {
         double ms = 0.0;
         for (size_t i = 0; i + 1 < h->ev_used[k]; i += 2) {
             float x = 0.f;
@@ -553,10 +636,10 @@ MBERT_API int mbert_attn_profile_read(mbert_attn *h, double *attn_ms, int64_t *a
                 return MBERT_ERR_CUDA;
             ms += x;
         }
-        if (attn_ms)
-            attn_ms[k] = ms;
-        if (attn_launches)
-            attn_launches[k] = static_cast<int64_t>(h->ev_used[k] / 2);
+        if (kernel_ms)
+            kernel_ms[k] = ms;
+        if (kernel_launches)
+            kernel_launches[k] = static_cast<int64_t>(h->ev_used[k] / 2);
         h->ev_used[k] = 0;
     }
     if (total_launches)

@@ -98,6 +98,21 @@ struct LocalArgs {
 // tiles of keys per unit.
 cudaError_t launch_attn_local(const LocalArgs &a, cudaStream_t stream);
 
+// Output projection with the residual add, y = x + a Wo^T: persistent pairs
+// of CTAs over 256 x 256 output blocks.
+struct OutProjArgs {
+    CUtensorMap tm_a;            // a  [T][768], box 64 x 128, 128B swizzle
+    CUtensorMap tm_w;            // Wo [768][768] ([out][in]), box 64 x 128, 128B swizzle
+    CUtensorMap tm_x;            // x  [T][768], box 64 x 128, 128B swizzle
+    CUtensorMap tm_y;            // y  [T][768] (may be x), box 64 x 128, 128B swizzle
+    const __nv_bfloat16 *x;      // x itself, for L2 prefetches
+    long long T;
+    int num_ctas;                // SMs: the launch sizes its pairs by occupancy
+    int32_t *err;
+};
+
+cudaError_t launch_out_proj(const OutProjArgs &a, cudaStream_t stream);
+
 // Number of sequences up to which the local kernel finds its blocks itself
 // (above it the plan kernel writes a work list first).
 constexpr int kLocalSelfScheduleMaxSeqs = 256;

@@ -119,6 +119,25 @@ int mbert_attn_key_counts(mbert_attn *h, const int32_t *cu_seqlens, int n_seqs,
                           int64_t total_tokens, int max_seqlen, int layer_kind,
                           int32_t *counts, void *stream);
 
+/* The step after the attention block: the output projection with the
+ * residual add, y = x + a Wo^T ("ModernBERT-base Architecture Teardown",
+ * "How Does ModernBERT Make Q, K and V?": Wo maps the joined heads back from
+ * 768 to 768, stored [out, in]; "ModernBertModel", "Implementing it":
+ * x = x + a Wo^T).
+ *   a   device bf16 [total_tokens][768], row-major: the attention block's out.
+ *   wo  device bf16 [768][768], row-major, [out][in].
+ *   x   device bf16 [total_tokens][768], row-major: the residual stream.
+ *   y   device bf16 [total_tokens][768], row-major: written.  y may be x
+ *       itself (in-place update); it must not overlap a or wo, and must
+ *       overlap x either exactly or not at all.
+ * Products accumulate in fp32; y is rounded to bf16 (nearest even) once.
+ * All pointers 16-byte aligned; the caller owns every buffer.  Returns
+ * MBERT_OK; MBERT_ERR_BAD_ARG for a null handle or buffer, a misaligned or
+ * overlapping buffer, or total_tokens outside [0, 2^31); MBERT_ERR_CUDA on a
+ * launch failure.  Device timeouts are reported by mbert_attn_get_error(). */
+int mbert_attn_out_proj(mbert_attn *h, const void *a, const void *wo, const void *x,
+                        int64_t total_tokens, void *y, void *stream);
+
 /* Wait for the handle's most recent stream, then return (and clear) the
  * device error word as a status: MBERT_OK, MBERT_ERR_BAD_CU_SEQLENS,
  * MBERT_ERR_SEQ_TOO_LONG or MBERT_ERR_TIMEOUT; MBERT_ERR_CUDA if the wait
@@ -164,17 +183,24 @@ int mbert_attn_forward_noalloc(const void *qkv, const int32_t *cu_seqlens, int n
 
 /* Measurement.  While enabled, every mbert_attn_forward also records a
  * CUDA event pair on its stream around its attention kernel (the plan and
- * RoPE kernels before it are outside the pair).  The handle always counts
- * the kernels it enqueues. */
+ * RoPE kernels before it are outside the pair), and every
+ * mbert_attn_out_proj one around its kernel.  The handle always counts the
+ * kernels it enqueues. */
 int mbert_attn_profile_enable(mbert_attn *h, int enable);
 
-/* Synchronise on the recorded events and return, per layer kind
- * (index MBERT_GLOBAL / MBERT_LOCAL of the host arrays attn_ms[2] and
- * attn_launches[2]), the summed attention-kernel milliseconds and the number
- * of recorded kernels, plus the number of kernels enqueued by every entry
- * point (*total_launches).  Clears all three.  Any output pointer may be
- * NULL. */
-int mbert_attn_profile_read(mbert_attn *h, double *attn_ms, int64_t *attn_launches,
+/* Profile slots: the two layer kinds, then the output projection. */
+enum {
+    MBERT_PROFILE_OUT_PROJ = 2,
+    MBERT_PROFILE_SLOTS = 3
+};
+
+/* Synchronise on the recorded events and return, per profile slot (index
+ * MBERT_GLOBAL, MBERT_LOCAL or MBERT_PROFILE_OUT_PROJ of the host arrays
+ * kernel_ms[3] and kernel_launches[3]), the summed kernel milliseconds and
+ * the number of recorded kernels, plus the number of kernels enqueued by
+ * every entry point (*total_launches).  Clears all three.  Any output
+ * pointer may be NULL. */
+int mbert_attn_profile_read(mbert_attn *h, double *kernel_ms, int64_t *kernel_launches,
                             int64_t *total_launches);
 
 /* Release the handle's device memory.  NULL is allowed.  The caller must
