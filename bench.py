@@ -48,10 +48,12 @@ N_SETS = 6
 # profiles/attn_{global,local}_kernel_config3.md.  Reported only while the
 # kernel sources still hash to what was captured.
 NCU_TRAFFIC = {
-    "global": {"bytes": 39.98e6, "kernel": "attn_global_kernel",
-               "sources": {"attn_global.cu": "89c3d2ad0d680903", "common.cuh": "42f2174ca3b5eb40"}},
-    "local": {"bytes": 37.85e6, "kernel": "attn_local_kernel",
-              "sources": {"attn_local.cu": "0bc14693bd260833", "common.cuh": "42f2174ca3b5eb40"}},
+    "global": {"bytes": 39.64e6, "kernel": "attn_global_kernel",
+               "sources": {"attn_global.cu": "89c3d2ad0d680903", "common.cuh": "c49de87f54892de8"}},
+    "local": {"bytes": 37.83e6, "kernel": "attn_local_kernel",
+              "sources": {"attn_local.cu": "10494098048f75a4", "common.cuh": "c49de87f54892de8"}},
+    "out_proj": {"bytes": 26.38e6, "kernel": "out_proj_kernel",
+                 "sources": {"out_proj.cu": "a90b9f6fda100937", "common.cuh": "c49de87f54892de8"}},
 }
 
 WORKLOADS = {
@@ -95,8 +97,9 @@ def load_peaks():
 
 
 def captured_traffic(kind, workload):
-    """DRAM bytes per launch of the layer's attention kernel, or None if the
-    capture does not apply (another workload, or the kernel source changed)."""
+    """DRAM bytes per launch of a kernel ("global" / "local": the layer's
+    attention kernel; "out_proj": the projection), or None if the capture
+    does not apply (another workload, or the kernel source changed)."""
     import hashlib
     rec = NCU_TRAFFIC[kind]
     if workload != "config3":
@@ -413,6 +416,7 @@ def run_ours(args):
                 "tflops": pf / (proj_ms / 1e3) / 1e12, "hbm_gbs": pb / (proj_ms / 1e3) / 1e9,
                 "bound": "hbm" if pb / (peaks["hbm_gbs"] * 1e9) >= pf / (peaks["bf16_tflops"] * 1e12) else "tensor",
                 "roofline_frac": p_roof / (proj_ms / 1e3), "gflop": pf / 1e9, "mbytes": pb / 1e6,
+                "traffic": captured_traffic("out_proj", args.workload),
                 "note": "y = x + out Wo^T after the global layer, timed alone over "
                         f"{kp} calls enqueued ahead of the GPU: kernel_ms from a CUDA event "
                         "pair around each launch, ms_per_call from one pair around all "
