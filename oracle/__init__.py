@@ -13,6 +13,7 @@ path:
 * same page, "What Are Local and Global Attention?" and "ModernBERT"
   (candding), "The alternating attention": local layers keep |i - j| <= 64.
 * teardown, "How Does ModernBERT Make Q, K and V?": 12 heads of 64.
+* teardown, "What Does LayerNorm Do?": eps 1e-5 under the square root.
 """
 import ctypes
 import os
@@ -26,6 +27,7 @@ HEAD_DIM = 64
 GLOBAL = {"theta": 160000.0, "half_window": -1}
 LOCAL = {"theta": 10000.0, "half_window": 64}
 KINDS = {"global": GLOBAL, "local": LOCAL}
+NORM_EPS = 1e-5
 
 _lib = None
 
@@ -56,6 +58,12 @@ def lib():
         L.oracle_out_proj.argtypes = [u16p, u16p, u16p, ctypes.c_int64, ctypes.c_int, i64p,
                                       ctypes.c_int64, dp, ctypes.c_int]
         L.oracle_out_proj.restype = ctypes.c_int
+        L.oracle_layernorm.argtypes = [u16p, u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_double,
+                                       i64p, ctypes.c_int64, dp, ctypes.c_int]
+        L.oracle_layernorm.restype = ctypes.c_int
+        L.oracle_ln_qkv.argtypes = [u16p, u16p, u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_double, i64p, ctypes.c_int64, dp, ctypes.c_int]
+        L.oracle_ln_qkv.restype = ctypes.c_int
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = ctypes.c_int
         _lib = L
@@ -179,6 +187,68 @@ def out_proj(a_bits, wo_bits, x_bits, rows=None, threads: int = 0):
     if rc:
         raise ValueError(f"oracle_out_proj failed (code {rc})")
     return y
+
+
+def _rows_arg(rows, T):
+    if rows is None:
+        return T, None, None
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    return r.shape[0], r, _ptr(r, ctypes.c_int64)
+
+
+def layernorm(x_bits, w_bits=None, eps: float = NORM_EPS, rows=None, threads: int = 0):
+    """Bias-free LayerNorm in fp64, row by row; w_bits None is the identity
+    (layer 0's attn_norm).
+
+    x_bits: uint16 [T, d] bf16 bit patterns; w_bits: uint16 [d] or None.
+    Returns fp64 [n, d] (rows: None for every row, or sorted row indices).
+    """
+    x = np.ascontiguousarray(x_bits)
+    if x.dtype != np.uint16 or x.ndim != 2:
+        raise TypeError("x must be uint16 [T, d] bf16 bit patterns")
+    T, d = x.shape
+    wp = None
+    if w_bits is not None:
+        w = np.ascontiguousarray(w_bits)
+        if w.dtype != np.uint16 or w.shape != (d,):
+            raise TypeError("w must be uint16 [d] bf16 bit patterns")
+        wp = _ptr(w, ctypes.c_uint16)
+    n, r, rp = _rows_arg(rows, T)
+    h = np.empty((n, d), dtype=np.float64)
+    rc = lib().oracle_layernorm(_ptr(x, ctypes.c_uint16), wp, T, d, float(eps), rp, n,
+                                _ptr(h, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError(f"oracle_layernorm failed (code {rc})")
+    return h
+
+
+def ln_qkv(x_bits, w_bits, wqkv_bits, eps: float = NORM_EPS, rows=None, threads: int = 0):
+    """qkv = LayerNorm(x) Wqkv^T in fp64 (Wqkv stored [out][in]); w_bits None
+    is the identity norm of layer 0.
+
+    x_bits: uint16 [T, d]; w_bits: uint16 [d] or None; wqkv_bits: uint16
+    [n_out, d].  Returns fp64 [n, n_out].
+    """
+    x = np.ascontiguousarray(x_bits)
+    wq = np.ascontiguousarray(wqkv_bits)
+    if x.dtype != np.uint16 or wq.dtype != np.uint16 or x.ndim != 2 or wq.ndim != 2:
+        raise TypeError("x and wqkv must be 2-D uint16 bf16 bit patterns")
+    T, d = x.shape
+    n_out = wq.shape[0]
+    assert wq.shape == (n_out, d)
+    wp = None
+    if w_bits is not None:
+        w = np.ascontiguousarray(w_bits)
+        if w.dtype != np.uint16 or w.shape != (d,):
+            raise TypeError("w must be uint16 [d] bf16 bit patterns")
+        wp = _ptr(w, ctypes.c_uint16)
+    n, r, rp = _rows_arg(rows, T)
+    out = np.empty((n, n_out), dtype=np.float64)
+    rc = lib().oracle_ln_qkv(_ptr(x, ctypes.c_uint16), wp, _ptr(wq, ctypes.c_uint16), T, d,
+                             n_out, float(eps), rp, n, _ptr(out, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError(f"oracle_ln_qkv failed (code {rc})")
+    return out
 
 
 def attention_kind(qkv_bits, cu_seqlens, kind: str, rows=None, threads: int = 0):

@@ -484,6 +484,105 @@ int oracle_out_proj(const uint16_t *a, const uint16_t *wo, const uint16_t *x, in
     return bad ? -3 : 0;
 }
 
+/* ------------------------------------------------------------------ */
+/* pre-attention LayerNorm and the fused Wqkv projection               */
+/* ------------------------------------------------------------------ */
+
+/* One row of the bias-free LayerNorm ("ModernBERT-base Architecture
+ * Teardown", "What Does LayerNorm Do?"): subtract the row mean, divide by the
+ * population standard deviation with eps added under the square root, then
+ * multiply position c by the learned weight w[c]; no bias.  w == NULL is
+ * layer 0's attn_norm, an identity ("What Does LayerNorm Do?"; "ModernBERT"
+ * (candding), "The pre-norm layer and the final norm"): h = x.  x and w are
+ * bf16 bit patterns; h is fp64 [d]. */
+static void layernorm_row(const uint16_t *x, const uint16_t *w, int d, double eps, double *h)
+{
+    if (!w) {
+        for (int c = 0; c < d; c++)
+            h[c] = bf16_to_f64(x[c]);
+        return;
+    }
+    double sum = 0.0;
+    for (int c = 0; c < d; c++)
+        sum += bf16_to_f64(x[c]);
+    const double mean = sum / d;
+    double sq = 0.0;
+    for (int c = 0; c < d; c++) {
+        const double dev = bf16_to_f64(x[c]) - mean;
+        sq += dev * dev;
+    }
+    const double sd = sqrt(sq / d + eps);
+    for (int c = 0; c < d; c++)
+        h[c] = (bf16_to_f64(x[c]) - mean) / sd * bf16_to_f64(w[c]);
+}
+
+/* h = LayerNorm(x) row by row, fp64 [n][d] (rows: NULL for every row, or n
+ * sorted row indices). */
+int oracle_layernorm(const uint16_t *x, const uint16_t *w, int64_t T, int d, double eps,
+                     const int64_t *rows, int64_t n, double *h, int threads)
+{
+    if (T < 0 || d <= 0 || n < 0 || eps < 0.0)
+        return -1;
+    if (!rows)
+        n = T;
+    int bad = 0;
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : oracle_max_threads()) reduction(|:bad)
+    for (int64_t k = 0; k < n; k++) {
+        const int64_t t = rows ? rows[k] : k;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        layernorm_row(x + t * d, w, d, eps, h + k * d);
+    }
+    return bad ? -3 : 0;
+}
+
+/* qkv[t][j] = sum_c h[t][c] * wqkv[j][c] with h = LayerNorm(x) (w == NULL:
+ * h = x), j = 0 .. n_out - 1: the attention block's input, made by the fused
+ * Wqkv, a bias-free Linear weight stored [out][in] = [3 * d][d]
+ * ("ModernBERT-base Architecture Teardown", "How Does ModernBERT Make Q, K
+ * and V?"; "ModernBertModel" (safebydesign), "Implementing it": the norm's
+ * output times Wqkv^T, split three ways).  Every sum in fp64, no intermediate
+ * rounding; qkv is fp64 [n][n_out]. */
+int oracle_ln_qkv(const uint16_t *x, const uint16_t *w, const uint16_t *wqkv, int64_t T, int d,
+                  int n_out, double eps, const int64_t *rows, int64_t n, double *qkv, int threads)
+{
+    if (T < 0 || d <= 0 || n_out <= 0 || n < 0 || eps < 0.0)
+        return -1;
+    if (!rows)
+        n = T;
+    double *wm = malloc(sizeof(double) * (size_t)n_out * (size_t)d);
+    if (!wm)
+        return -2;
+    for (int64_t e = 0; e < (int64_t)n_out * d; e++)
+        wm[e] = bf16_to_f64(wqkv[e]);
+    int bad = 0;
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : oracle_max_threads()) reduction(|:bad)
+    for (int64_t k = 0; k < n; k++) {
+        const int64_t t = rows ? rows[k] : k;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        double *h = malloc(sizeof(double) * (size_t)d);
+        if (!h) {
+            bad = 1;
+            continue;
+        }
+        layernorm_row(x + t * d, w, d, eps, h);
+        for (int j = 0; j < n_out; j++) {
+            double acc = 0.0;
+            for (int c = 0; c < d; c++)
+                acc += h[c] * wm[(int64_t)j * d + c];
+            qkv[k * n_out + j] = acc;
+        }
+        free(h);
+    }
+    free(wm);
+    return bad ? -3 : 0;
+}
+
 /* Number of OpenMP threads a parallel region would use by default. */
 int oracle_max_threads(void)
 {

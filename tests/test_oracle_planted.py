@@ -1,5 +1,6 @@
 """Planted mistakes: each plausible error, put into a copy of the oracle on
-the CPU, must make at least one pin of test_oracle.py fail.
+the CPU, must make at least one pin (test_oracle.py, test_oracle_out_proj.py,
+test_oracle_ln_qkv.py) fail.
 
 The copy is made by a textual edit of the oracle's C source, compiled into a
 temporary library and swapped in for the duration of the check; the oracle
@@ -15,6 +16,7 @@ import oracle
 from oracle import build as obuild
 import test_oracle as T
 import test_oracle_out_proj as P
+import test_oracle_ln_qkv as N
 
 # (name, original source fragment, planted fragment)
 PLANTS = [
@@ -34,7 +36,22 @@ PLANTS = [
      "acc += ar[c] * w[(int64_t)c * d + o];"),
     ("out_proj_without_residual", "y[k * d + o] = bf16_to_f64(x[t * d + o]) + acc;",
      "y[k * d + o] = acc;"),
+    ("ln_unbiased_variance", "const double sd = sqrt(sq / d + eps);",
+     "const double sd = sqrt(sq / (d - 1) + eps);"),
+    ("ln_eps_outside_sqrt", "const double sd = sqrt(sq / d + eps);",
+     "const double sd = sqrt(sq / d) + eps;"),
+    ("ln_mean_not_subtracted", "h[c] = (bf16_to_f64(x[c]) - mean) / sd * bf16_to_f64(w[c]);",
+     "h[c] = bf16_to_f64(x[c]) / sd * bf16_to_f64(w[c]);"),
+    ("ln_weight_ignored", "h[c] = (bf16_to_f64(x[c]) - mean) / sd * bf16_to_f64(w[c]);",
+     "h[c] = (bf16_to_f64(x[c]) - mean) / sd;"),
+    ("qkv_weight_transposed", "acc += h[c] * wm[(int64_t)j * d + c];",
+     "acc += h[c] * wm[(int64_t)c * n_out + j];"),
 ]
+
+# every exported function whose ctypes signature the copies must share
+_FUNCS = ("oracle_inv_freq", "oracle_rope_row", "oracle_key_counts", "oracle_sdpa_dense",
+          "oracle_attention", "oracle_out_proj", "oracle_layernorm", "oracle_ln_qkv",
+          "oracle_max_threads")
 
 
 def _pins():
@@ -54,6 +71,11 @@ def _pins():
     ]
     out += [P.test_hand_worked_example, P.test_permutation_weight_permutes_columns,
             P.test_zero_weight_returns_the_residual, P.test_power_of_two_diagonal]
+    out += [N.test_page_worked_example, N.test_mean_zero_and_spread_closed_form,
+            N.test_constant_row_gives_zero, N.test_scale_invariance_without_eps,
+            N.test_shift_invariance_on_integers, N.test_weight_scales_positions,
+            N.test_matches_torch_layer_norm, N.test_ln_qkv_equals_library_matmul,
+            N.test_identity_norm_of_layer_zero, N.test_three_way_split_with_selection_weights]
     out += [(lambda r=r: T.test_key_counts_match_pages(r)) for r in table]
     for lengths in ([5, 64, 65], [130, 7, 200]):
         for kind in ("global", "local"):
@@ -77,8 +99,7 @@ def test_planted_mistake_fails_a_pin(tmp_path, name, original, planted):
     good = oracle.lib()
     libpath = _compile_variant(tmp_path, original, planted)
     bad = ctypes.CDLL(libpath)
-    for fn in ("oracle_inv_freq", "oracle_rope_row", "oracle_key_counts",
-               "oracle_sdpa_dense", "oracle_attention", "oracle_max_threads"):
+    for fn in _FUNCS:
         getattr(bad, fn).argtypes = getattr(good, fn).argtypes
         getattr(bad, fn).restype = getattr(good, fn).restype
     failed = []
@@ -104,8 +125,7 @@ def test_unplanted_copy_passes_every_pin(tmp_path):
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-shared",
                     "-fPIC", "-o", str(lib), str(path), "-lm"], check=True)
     copy = ctypes.CDLL(str(lib))
-    for fn in ("oracle_inv_freq", "oracle_rope_row", "oracle_key_counts",
-               "oracle_sdpa_dense", "oracle_attention", "oracle_max_threads"):
+    for fn in _FUNCS:
         getattr(copy, fn).argtypes = getattr(good, fn).argtypes
         getattr(copy, fn).restype = getattr(good, fn).restype
     oracle._lib = copy
