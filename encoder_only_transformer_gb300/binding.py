@@ -20,6 +20,7 @@ _KINDS = {"global": GLOBAL, "local": LOCAL, GLOBAL: GLOBAL, LOCAL: LOCAL}
 
 HEADS, HEAD_DIM = 12, 64
 QKV_WIDTH, OUT_WIDTH = 3 * HEADS * HEAD_DIM, HEADS * HEAD_DIM
+NORM_EPS = 1e-5   # LayerNorm eps of ModernBERT-base (teardown, "What Does LayerNorm Do?")
 
 # Every symbol the public header declares, with its ctypes signature.
 _c_int, _c_i64, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
@@ -38,6 +39,7 @@ SIGNATURES = {
     "mbert_attn_forward": (_c_int, [_vp, _vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp]),
     "mbert_attn_key_counts": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp]),
     "mbert_attn_out_proj": (_c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _vp]),
+    "mbert_attn_ln_qkv": (_c_int, [_vp, _vp, _vp, _vp, _c_i64, ctypes.c_float, _vp, _vp]),
     "mbert_attn_get_error": (_c_int, [_vp]),
     "mbert_attn_selftest_timeout": (_c_int, [_vp, _c_i64, _vp]),
     "mbert_attn_forward_noalloc": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp,
@@ -198,6 +200,29 @@ class Attention:
         _check(st, "out_proj")
         return out
 
+    def ln_qkv(self, x: torch.Tensor, norm_w, wqkv: torch.Tensor, eps: float = NORM_EPS,
+               out: torch.Tensor = None) -> torch.Tensor:
+        """qkv[T, 2304] bf16 = LayerNorm(x) Wqkv^T: the bias-free pre-attention
+        norm (weight norm_w [768], or None for layer 0's identity) and the
+        fused Wqkv projection (Wqkv [2304, 768], stored [out, in])."""
+        def check(t, name, shape):
+            if (t.dtype != torch.bfloat16 or tuple(t.shape) != shape or t.device != self.device
+                    or not t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous bf16 {list(shape)} tensor on {self.device}")
+        T = x.shape[0] if x.dim() == 2 else -1
+        check(x, "x", (T, OUT_WIDTH))
+        if norm_w is not None:
+            check(norm_w, "norm_w", (OUT_WIDTH,))
+        check(wqkv, "wqkv", (QKV_WIDTH, OUT_WIDTH))
+        if out is None:
+            out = torch.empty(T, QKV_WIDTH, dtype=torch.bfloat16, device=self.device)
+        check(out, "out", (T, QKV_WIDTH))
+        st = load_library().mbert_attn_ln_qkv(
+            self._h, x.data_ptr(), None if norm_w is None else norm_w.data_ptr(), wqkv.data_ptr(),
+            T, float(eps), out.data_ptr(), _stream_ptr(self.device))
+        _check(st, "ln_qkv")
+        return out
+
     def key_counts(self, cu_seqlens: torch.Tensor, total_tokens: int, layer_kind,
                    max_seqlen: int = 0) -> torch.Tensor:
         """int32 [T]: keys the kernels' schedule and mask admit per query row."""
@@ -217,18 +242,19 @@ class Attention:
                "selftest_timeout")
 
     def profile(self, enable: bool = True):
-        """Record a CUDA event pair around every attention and projection kernel."""
+        """Record a CUDA event pair around every attention, projection and norm kernel."""
         _check(load_library().mbert_attn_profile_enable(self._h, 1 if enable else 0), "profile")
 
     def profile_read(self):
-        """-> ({'global': ms, 'local': ms, 'out_proj': ms}, the same keys -> kernel
-        count, total_launches); synchronises and clears the record."""
-        ms = (ctypes.c_double * 3)()
-        n = (ctypes.c_int64 * 3)()
+        """-> ({'global': ms, 'local': ms, 'out_proj': ms, 'qkv_proj': ms,
+        'layernorm': ms}, the same keys -> kernel count, total_launches);
+        synchronises and clears the record."""
+        keys = ("global", "local", "out_proj", "qkv_proj", "layernorm")
+        ms = (ctypes.c_double * len(keys))()
+        n = (ctypes.c_int64 * len(keys))()
         tot = ctypes.c_int64()
         _check(load_library().mbert_attn_profile_read(self._h, ms, n, ctypes.byref(tot)),
                "profile_read")
-        keys = ("global", "local", "out_proj")
         return ({k: ms[i] for i, k in enumerate(keys)}, {k: n[i] for i, k in enumerate(keys)},
                 int(tot.value))
 
@@ -256,6 +282,15 @@ def attention(qkv: torch.Tensor, cu_seqlens: torch.Tensor, layer_kind, max_seqle
     if not qkv.is_cuda:
         raise ValueError("qkv must be a CUDA tensor")
     return _default(qkv.device).forward(qkv, cu_seqlens, layer_kind, max_seqlen, out)
+
+
+def ln_qkv(x: torch.Tensor, norm_w, wqkv: torch.Tensor, eps: float = NORM_EPS,
+           out: torch.Tensor = None) -> torch.Tensor:
+    """qkv = LayerNorm(x) Wqkv^T (bf16, CUDA tensors; norm_w None on layer 0):
+    the step before the attention block."""
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    return _default(x.device).ln_qkv(x, norm_w, wqkv, eps, out)
 
 
 def out_proj(a: torch.Tensor, wo: torch.Tensor, x: torch.Tensor, out: torch.Tensor = None) -> torch.Tensor:

@@ -33,6 +33,8 @@ struct mbert_attn {
     int64_t work_cap = 0;                   // entries
     __nv_bfloat16 *rot = nullptr;           // rotated Q/K scratch [rows][1536]
     int64_t rot_cap = 0;                    // rows
+    __nv_bfloat16 *ln = nullptr;            // normalised rows [ln_cap][768] (ln_qkv)
+    int64_t ln_cap = 0;                     // rows
     // global layers: split of the (entry, head, key tile) iterations among
     // one persistent CTA per SM
     int32_t *tile_start = nullptr;          // [entries + 1]
@@ -144,6 +146,7 @@ int grow_workspace(mbert_attn *h, int64_t entries, int64_t rot_rows)
         if (h->rot) {
             cudaDeviceSynchronize();
             cudaFree(h->rot);
+        cudaFree(h->ln);
         }
         h->rot = r;
         h->rot_cap = cap;
@@ -572,6 +575,82 @@ MBERT_API int mbert_attn_out_proj(mbert_attn *h, const void *a, const void *wo, 
     cudaError_t e = ev0 ? cudaEventRecord(ev0, st) : cudaSuccess;
     if (e == cudaSuccess)
         e = launch_out_proj(o, st);
+    if (e == cudaSuccess && ev1)
+        e = cudaEventRecord(ev1, st);
+    h->launches += 1;
+    h->last_stream = st;
+    return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
+}
+
+MBERT_API int mbert_attn_ln_qkv(mbert_attn *h, const void *x, const void *norm_w, const void *wqkv,
+                                int64_t total_tokens, float eps, void *qkv, void *stream)
+{
+    if (!h || total_tokens < 0 || total_tokens > INT32_MAX || !(eps >= 0.f) || eps > 1.f)
+        return MBERT_ERR_BAD_ARG;
+    const int64_t T = total_tokens;
+    if (T == 0)
+        return MBERT_OK;
+    if (!x || !wqkv || !qkv)
+        return MBERT_ERR_BAD_ARG;
+    for (const void *ptr : {x, norm_w, wqkv, static_cast<const void *>(qkv)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15)
+            return MBERT_ERR_BAD_ARG;
+    const size_t xbytes = static_cast<size_t>(T) * kHidden * 2;
+    const size_t qbytes = static_cast<size_t>(T) * kQKVWidth * 2;
+    const size_t wbytes = static_cast<size_t>(kQKVWidth) * kHidden * 2;
+    if (ranges_overlap(x, xbytes, qkv, qbytes) || ranges_overlap(wqkv, wbytes, qkv, qbytes) ||
+        (norm_w && ranges_overlap(norm_w, kHidden * 2, qkv, qbytes)))
+        return MBERT_ERR_BAD_ARG;
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const void *a = x;
+    if (norm_w) {
+        if (T > h->ln_cap) {
+            const int64_t cap = T < 8192 ? 8192 : T;
+            __nv_bfloat16 *buf = nullptr;
+            if (cudaMalloc(&buf, sizeof(__nv_bfloat16) * kHidden * cap) != cudaSuccess) {
+                cudaGetLastError();
+                return MBERT_ERR_OOM;
+            }
+            if (h->ln) {
+                cudaDeviceSynchronize();
+                cudaFree(h->ln);
+            }
+            h->ln = buf;
+            h->ln_cap = cap;
+        }
+        a = h->ln;
+    }
+    QkvProjArgs q;
+    if (encode_map(h, &q.tm_a, a, kHidden, T) != MBERT_OK ||
+        encode_map(h, &q.tm_w, wqkv, kHidden, kQKVWidth) != MBERT_OK ||
+        encode_map(h, &q.tm_y, qkv, kQKVWidth, T) != MBERT_OK)
+        return MBERT_ERR_CUDA;
+    q.T = T;
+    q.num_ctas = h->num_sms;
+    q.err = h->err;
+    cudaError_t e = cudaSuccess;
+    if (norm_w) {
+        cudaEvent_t l0, l1;
+        if (profile_events(h, MBERT_PROFILE_LAYERNORM, &l0, &l1) != MBERT_OK)
+            return MBERT_ERR_CUDA;
+        if (l0)
+            e = cudaEventRecord(l0, st);
+        if (e == cudaSuccess)
+            e = launch_layernorm(static_cast<const __nv_bfloat16 *>(x),
+                                 static_cast<const __nv_bfloat16 *>(norm_w), T, eps, h->ln,
+                                 h->num_sms, st);
+        if (e == cudaSuccess && l1)
+            e = cudaEventRecord(l1, st);
+        h->launches += 1;
+    }
+    cudaEvent_t ev0, ev1;
+    if (e == cudaSuccess && profile_events(h, MBERT_PROFILE_QKV_PROJ, &ev0, &ev1) != MBERT_OK)
+        return MBERT_ERR_CUDA;
+    if (e == cudaSuccess && ev0)
+        e = cudaEventRecord(ev0, st);
+    if (e == cudaSuccess)
+        e = launch_qkv_proj(q, st);
     if (e == cudaSuccess && ev1)
         e = cudaEventRecord(ev1, st);
     h->launches += 1;

@@ -113,6 +113,24 @@ struct OutProjArgs {
 
 cudaError_t launch_out_proj(const OutProjArgs &a, cudaStream_t stream);
 
+// The fused Wqkv projection, qkv = h Wqkv^T: the same paired GEMM over
+// 256 x 256 output blocks, 2304 output columns, no residual.
+struct QkvProjArgs {
+    CUtensorMap tm_a;            // h    [T][768], box 64 x 128, 128B swizzle
+    CUtensorMap tm_w;            // Wqkv [2304][768] ([out][in]), box 64 x 128, 128B swizzle
+    CUtensorMap tm_y;            // qkv  [T][2304], box 64 x 128, 128B swizzle
+    long long T;
+    int num_ctas;
+    int32_t *err;
+};
+
+cudaError_t launch_qkv_proj(const QkvProjArgs &a, cudaStream_t stream);
+
+// Bias-free LayerNorm of each row of x [T][768] (bf16) with weight w [768]
+// into h [T][768] (bf16): one warp per row, fp32 statistics.
+cudaError_t launch_layernorm(const __nv_bfloat16 *x, const __nv_bfloat16 *w, long long T,
+                             float eps, __nv_bfloat16 *h, int num_sms, cudaStream_t stream);
+
 // Number of sequences up to which the local kernel finds its blocks itself
 // (above it the plan kernel writes a work list first).
 constexpr int kLocalSelfScheduleMaxSeqs = 256;

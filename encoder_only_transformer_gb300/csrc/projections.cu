@@ -1,11 +1,16 @@
-// Output projection with the residual add, y = x + a Wo^T (tcgen05 + TMA,
-// sm_103a).
+// The block's two projections, as paired-SM GEMMs (tcgen05 + TMA, sm_103a):
 //
-// a: the joined head outputs of the attention block, bf16 [T][768]; Wo:
-// bf16 [768][768] stored [out][in] ("ModernBERT-base Architecture Teardown",
-// "How Does ModernBERT Make Q, K and V?": Wo maps the joined heads back from
-// 768 to 768); x: the residual stream, bf16 [T][768]; y = x + a Wo^T
-// ("ModernBertModel", "Implementing it"), bf16, fp32 accumulation.
+//  * qkv_proj_kernel: qkv = h Wqkv^T, h bf16 [T][768] (the pre-attention
+//    LayerNorm's output, or x itself on layer 0), Wqkv bf16 [2304][768]
+//    stored [out][in] ("ModernBERT-base Architecture Teardown", "How Does
+//    ModernBERT Make Q, K and V?": Wqkv turns 768 numbers into 2304; the
+//    norm's output times Wqkv^T, "ModernBertModel", "Implementing it");
+//    qkv bf16 [T][2304].
+//  * out_proj_kernel: y = x + a Wo^T, a the joined head outputs bf16
+//    [T][768], Wo bf16 [768][768] stored [out][in] (same section: Wo maps
+//    the joined heads back from 768 to 768), x the residual stream bf16
+//    [T][768] ("Implementing it": x = x + a Wo^T); y bf16 [T][768].
+// Both accumulate in fp32 and round once to bf16; K = 768.
 //
 // The tensor pipe of one SM takes 128 x N x 16 per 64 clocks at N = 128,
 // and an SM's copy engine delivers about 64 bytes per clock, which feeds a
@@ -17,19 +22,20 @@
 // Persistent pairs: each takes a contiguous run of units, a unit being 256
 // rows x 256 output columns (row-major over the units); CTA r of the pair
 // owns rows 128 r .. 128 r + 127 of the unit.  K = 768 is walked in 12 steps
-// of 64:
-//   warp 0      producer (both CTAs): TMA of the CTA's a box and Wo box
+// of 64 (A = the activations, B = the weight):
+//   warp 0      producer (both CTAs): TMA of the CTA's A box and B box
 //               (128 x 64 each, 128-byte swizzle) into a 5-stage ring, both
 //               completing the leader CTA's stage barrier
-//   warp 1      MMA issuer (leader CTA only): D (+)= a Wo^T over the pair
+//   warp 1      MMA issuer (leader CTA only): D (+)= A B^T over the pair
 //               into one of two 256-column TMEM accumulators per CTA; each
 //               stage's commit frees the stage in both CTAs
 //   warps 2-9   epilogue (both CTAs): warp w takes TMEM lane quadrant w % 4
-//               and column half (w - 2) / 4, one row per thread.  The unit's
-//               x arrives in the staging tile by TMA (fetched into L2 a unit
-//               ahead); y = D + x is written over it there and leaves by TMA
-//               stores that clip rows past T, after which the lead thread
-//               loads the next unit's x.
+//               and column half (w - 2) / 4, one row per thread; the output
+//               goes through a staging tile and TMA stores that clip rows
+//               past T.  With the residual, the unit's x first arrives in the
+//               staging tile by TMA (fetched into L2 a unit ahead) and
+//               y = D + x is written over it; the lead thread loads the next
+//               unit's x once the store has read the tile.
 // y may be x itself: a unit reads its x before its y is stored, and no other
 // unit touches those elements.
 #include "common.cuh"
@@ -46,9 +52,8 @@ constexpr int kUnitM = 2 * kBM;         // rows per unit (the pair)
 constexpr int kBN = 256;                // output columns per unit (MMA N)
 constexpr int kBK = 64;
 constexpr int kKSteps = kD / kBK;       // 12
-constexpr int kColBlocks = kD / kBN;    // 3
 constexpr int kStages = 5;
-constexpr uint32_t kStageBytes = 2 * kTileBytes;             // a box + Wo box (this CTA's half)
+constexpr uint32_t kStageBytes = 2 * kTileBytes;             // A box + B box (this CTA's half)
 constexpr uint32_t kOffRing = 0;
 constexpr uint32_t kOffY = kStages * kStageBytes;            // staging tile: 128 rows x 256 columns
 constexpr int kYBoxes = kBN / 64;
@@ -61,7 +66,8 @@ static_assert(kSmemBytes + 16 <= 227 * 1024, "shared memory");
 
 enum : int {
     kBarFull = 0, kBarEmpty = kStages, kBarAccFull = 2 * kStages, kBarAccEmpty = kBarAccFull + 2,
-    kBarXFull = kBarAccEmpty + 2, kBarYReady, kBarDrain,
+    kBarXFull = kBarAccEmpty + 2,  // residual: x landed; otherwise: the staging tile is free
+    kBarYReady, kBarDrain,
     kNumBars
 };
 
@@ -174,10 +180,29 @@ __device__ __forceinline__ void add_x_row(uint32_t rowp, int r, const uint32_t (
     }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
-                const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
-                const __nv_bfloat16 *x, long long T, int n_units, int32_t *err)
+// bf16(v) for one 64-column box row into the swizzled staging row.
+__device__ __forceinline__ void store_row(uint32_t rowp, int r, const uint32_t (&v)[2][32])
+{
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint32_t yw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            yw[e] = pack_bf16x2(__uint_as_float(v[c / 4][8 * (c % 4) + 2 * e]),
+                                __uint_as_float(v[c / 4][8 * (c % 4) + 2 * e + 1]));
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
+                     :: "r"(rowp + ((c ^ (r & 7)) << 4)), "r"(yw[0]), "r"(yw[1]), "r"(yw[2]), "r"(yw[3])
+                     : "memory");
+    }
+}
+
+// The kernel body: output columns in kColBlocks blocks of 256; with
+// kResidual, y = x + D, else y = D.
+template <int kColBlocks, bool kResidual>
+__device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtensorMap &tm_w,
+                                          const CUtensorMap &tm_x, const CUtensorMap &tm_y,
+                                          const __nv_bfloat16 *x, long long T, int n_units,
+                                          int32_t *err)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
@@ -200,7 +225,8 @@ out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     } else if (tid == 0) {
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_w);
-        tma_prefetch_desc(&tm_x);
+        if constexpr (kResidual)
+            tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_y);
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
@@ -298,7 +324,7 @@ out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         auto prefetch_x = [&](int i) {
             const long long row = static_cast<long long>(unit_m0(i)) + r;
             if (row < T)
-                l2_prefetch_bytes(x + static_cast<size_t>(row) * kD + unit_n0(i) + 128 * hf, 256);
+                l2_prefetch_bytes(x + static_cast<size_t>(row) * (kColBlocks * kBN) + unit_n0(i) + 128 * hf, 256);
         };
         auto load_x = [&](int i) {                     // unit i's x into the staging tile
             const uint32_t bar = barp(base, kBarXFull);
@@ -307,23 +333,33 @@ out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 tma_load_2d_hint(base + kOffY + b * kTileBytes, &tm_x, unit_n0(i) + 64 * b, unit_m0(i), bar, once);
         };
         int x_issued = 0, x_done = 0;
-        if (lead && my_units > 0) {
-            load_x(0);
-            x_issued = 1;
+        if constexpr (kResidual) {
+            if (lead && my_units > 0) {
+                load_x(0);
+                x_issued = 1;
+            }
         }
         bool ok = true;
         for (int i = 0; i < my_units && ok; ++i) {
-            if (i + 1 < my_units)
-                prefetch_x(i + 1);                     // a unit ahead of its load
+            if constexpr (kResidual) {
+                if (i + 1 < my_units)
+                    prefetch_x(i + 1);                 // a unit ahead of its load
+            }
             const int acc = i & 1;
-            if (!(ok = mbar_wait(barp(base, kBarAccFull + acc), static_cast<uint32_t>(i >> 1) & 1u, err) &&
-                       mbar_wait(barp(base, kBarXFull), static_cast<uint32_t>(i & 1), err)))
+            // the accumulator is complete; with the residual the unit's x has
+            // landed, otherwise the previous unit's store has read the tile
+            bool ready = mbar_wait(barp(base, kBarAccFull + acc), static_cast<uint32_t>(i >> 1) & 1u, err);
+            if constexpr (kResidual)
+                ready = ready && mbar_wait(barp(base, kBarXFull), static_cast<uint32_t>(i & 1), err);
+            else
+                ready = ready && (i == 0 || mbar_wait(barp(base, kBarXFull), static_cast<uint32_t>((i - 1) & 1), err));
+            if (!(ok = ready))
                 break;
             x_done = i + 1;
             __syncwarp();
             tc_fence_after();
             // box 2 hf + bb holds columns 64 (2 hf + bb) .. + 63; the second
-            // box's accumulator loads while the first is added
+            // box's accumulator loads while the first is written
             uint32_t va[2][32], vb[2][32];
             tmem_ld32(tmem + acc * kBN + lane_off + 128 * hf, va[0]);
             tmem_ld32(tmem + acc * kBN + lane_off + 128 * hf + 32, va[1]);
@@ -332,11 +368,17 @@ out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             reg_fence32(va[1]);
             tmem_ld32(tmem + acc * kBN + lane_off + 128 * hf + 64, vb[0]);
             tmem_ld32(tmem + acc * kBN + lane_off + 128 * hf + 96, vb[1]);
-            add_x_row(base + kOffY + (2 * hf) * kTileBytes + r * 128, r, va);
+            if constexpr (kResidual)
+                add_x_row(base + kOffY + (2 * hf) * kTileBytes + r * 128, r, va);
+            else
+                store_row(base + kOffY + (2 * hf) * kTileBytes + r * 128, r, va);
             tmem_wait_ld();
             reg_fence32(vb[0]);
             reg_fence32(vb[1]);
-            add_x_row(base + kOffY + (2 * hf + 1) * kTileBytes + r * 128, r, vb);
+            if constexpr (kResidual)
+                add_x_row(base + kOffY + (2 * hf + 1) * kTileBytes + r * 128, r, vb);
+            else
+                store_row(base + kOffY + (2 * hf + 1) * kTileBytes + r * 128, r, vb);
             // the accumulator may be reused: one arrival per warp at the leader
             tc_fence_before();
             __syncwarp();
@@ -353,16 +395,21 @@ out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                         tma_store_2d(&tm_y, base + kOffY + b * kTileBytes, unit_n0(i) + 64 * b, m0);
                     bulk_commit();
                 }
-                if (i + 1 < my_units) {
-                    bulk_wait_read0();                   // the store has read the staging tile
-                    load_x(i + 1);
-                    x_issued = i + 2;
+                if constexpr (kResidual) {
+                    if (i + 1 < my_units) {
+                        bulk_wait_read0();               // the store has read the staging tile
+                        load_x(i + 1);
+                        x_issued = i + 2;
+                    }
+                } else {
+                    bulk_wait_read0();
+                    mbar_arrive(barp(base, kBarXFull));  // the staging tile may be rewritten
                 }
             }
         }
         if (lead) {
             // an x load still in flight after a timeout lands before the exit
-            if (x_done < x_issued)
+            if (kResidual && x_done < x_issued)
                 mbar_wait(barp(base, kBarXFull), static_cast<uint32_t>((x_issued - 1) & 1), err, kDrainLimitNs);
             bulk_wait0();                                // the stores have completed
         }
@@ -376,37 +423,78 @@ out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     }
 }
 
-}  // namespace
-
-cudaError_t launch_out_proj(const OutProjArgs &a, cudaStream_t stream)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+                const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+                const __nv_bfloat16 *x, long long T, int n_units, int32_t *err)
 {
-    // per device: the shared-memory opt-in and how many pairs fit at once
-    static int max_pairs[64] = {};
+    pair_gemm<kHidden / kBN, true>(tm_a, tm_w, tm_x, tm_y, x, T, n_units, err);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+                const __grid_constant__ CUtensorMap tm_y, long long T, int n_units, int32_t *err)
+{
+    pair_gemm<kQKVWidth / kBN, false>(tm_a, tm_w, tm_y, tm_y, nullptr, T, n_units, err);
+}
+
+// Pairs of CTAs to launch for `kernel`: as many as fit at once (per device,
+// found once), at most one per unit.  Sets the shared-memory opt-in.
+template <typename Kernel>
+cudaError_t pair_count(Kernel kernel, int (&cache)[64], int num_ctas, long long n_units, int *pairs)
+{
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64)
         return cudaErrorInvalidDevice;
-    if (max_pairs[dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(out_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cache[dev] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kSmemBytes));
         if (e != cudaSuccess)
             return e;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * (a.num_ctas / 2));
+        cfg.gridDim = dim3(2 * (num_ctas / 2));
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = kSmemBytes;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, out_proj_kernel, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
         if (e != cudaSuccess)
             return e;
-        max_pairs[dev] = n > 0 ? n : 1;
+        cache[dev] = n > 0 ? n : 1;
     }
-    const long long n_units = ((a.T + kUnitM - 1) / kUnitM) * kColBlocks;
+    *pairs = static_cast<int>(n_units < cache[dev] ? n_units : cache[dev]);   // >= 1 unit each
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_out_proj(const OutProjArgs &a, cudaStream_t stream)
+{
+    static int max_pairs[64] = {};
+    const long long n_units = ((a.T + kUnitM - 1) / kUnitM) * (kHidden / kBN);
     if (n_units <= 0)
         return cudaSuccess;
-    const long long pairs = n_units < max_pairs[dev] ? n_units : max_pairs[dev];   // >= 1 unit each
-    out_proj_kernel<<<static_cast<int>(2 * pairs), kThreads, kSmemBytes, stream>>>(
+    int pairs = 0;
+    cudaError_t e = pair_count(out_proj_kernel, max_pairs, a.num_ctas, n_units, &pairs);
+    if (e != cudaSuccess)
+        return e;
+    out_proj_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(
         a.tm_a, a.tm_w, a.tm_x, a.tm_y, a.x, a.T, static_cast<int>(n_units), a.err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qkv_proj(const QkvProjArgs &a, cudaStream_t stream)
+{
+    static int max_pairs[64] = {};
+    const long long n_units = ((a.T + kUnitM - 1) / kUnitM) * (kQKVWidth / kBN);
+    if (n_units <= 0)
+        return cudaSuccess;
+    int pairs = 0;
+    cudaError_t e = pair_count(qkv_proj_kernel, max_pairs, a.num_ctas, n_units, &pairs);
+    if (e != cudaSuccess)
+        return e;
+    qkv_proj_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(
+        a.tm_a, a.tm_w, a.tm_y, a.T, static_cast<int>(n_units), a.err);
     return cudaGetLastError();
 }
 

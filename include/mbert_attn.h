@@ -119,6 +119,35 @@ int mbert_attn_key_counts(mbert_attn *h, const int32_t *cu_seqlens, int n_seqs,
                           int64_t total_tokens, int max_seqlen, int layer_kind,
                           int32_t *counts, void *stream);
 
+/* The step before the attention block: its input qkv from the residual
+ * stream x, qkv = LayerNorm(x) Wqkv^T.  The LayerNorm is bias-free: each
+ * row minus its mean, divided by sqrt(population variance + eps), times the
+ * weight ("ModernBERT-base Architecture Teardown", "What Does LayerNorm
+ * Do?"); layer 0 has no norm before attention ("ModernBERT" (candding), "The
+ * pre-norm layer and the final norm").  Wqkv turns 768 numbers into 2304 =
+ * (3, 12, 64), Q, K, V head by head (teardown, "How Does ModernBERT Make Q,
+ * K and V?"), the layout mbert_attn_forward reads.
+ *   x       device bf16 [total_tokens][768], row-major.
+ *   norm_w  device bf16 [768], the norm's weight; NULL for no norm
+ *           (layer 0: qkv = x Wqkv^T).
+ *   wqkv    device bf16 [2304][768], row-major, [out][in].
+ *   eps     added to the variance under the square root (1e-5 in
+ *           ModernBERT-base); 0 <= eps <= 1.
+ *   qkv     device bf16 [total_tokens][2304], row-major: written; must not
+ *           overlap x, norm_w or wqkv.
+ * The norm runs in fp32 and its output is rounded to bf16 (the GEMM's
+ * operand) in a handle-owned buffer of total_tokens x 768 (grown with
+ * cudaMalloc when a call needs more; mbert_attn_reserve does not size it);
+ * the products accumulate in fp32 and qkv is rounded to bf16 once.  All
+ * pointers 16-byte aligned; the caller owns every buffer.  Returns MBERT_OK;
+ * MBERT_ERR_BAD_ARG for a null handle or buffer, a misaligned or overlapping
+ * buffer, a bad eps or total_tokens outside [0, 2^31); MBERT_ERR_OOM if the
+ * buffer cannot grow; MBERT_ERR_CUDA on a launch failure.  Calls that share
+ * a handle must not overlap on the GPU (they share the buffer).  Device
+ * timeouts are reported by mbert_attn_get_error(). */
+int mbert_attn_ln_qkv(mbert_attn *h, const void *x, const void *norm_w, const void *wqkv,
+                      int64_t total_tokens, float eps, void *qkv, void *stream);
+
 /* The step after the attention block: the output projection with the
  * residual add, y = x + a Wo^T ("ModernBERT-base Architecture Teardown",
  * "How Does ModernBERT Make Q, K and V?": Wo maps the joined heads back from
@@ -183,20 +212,24 @@ int mbert_attn_forward_noalloc(const void *qkv, const int32_t *cu_seqlens, int n
 
 /* Measurement.  While enabled, every mbert_attn_forward also records a
  * CUDA event pair on its stream around its attention kernel (the plan and
- * RoPE kernels before it are outside the pair), and every
- * mbert_attn_out_proj one around its kernel.  The handle always counts the
- * kernels it enqueues. */
+ * RoPE kernels before it are outside the pair), every mbert_attn_out_proj
+ * one around its kernel, and every mbert_attn_ln_qkv one around each of its
+ * two kernels.  The handle always counts the kernels it enqueues. */
 int mbert_attn_profile_enable(mbert_attn *h, int enable);
 
-/* Profile slots: the two layer kinds, then the output projection. */
+/* Profile slots: the two layer kinds, the output projection, the Wqkv
+ * projection and the pre-attention LayerNorm. */
 enum {
     MBERT_PROFILE_OUT_PROJ = 2,
-    MBERT_PROFILE_SLOTS = 3
+    MBERT_PROFILE_QKV_PROJ = 3,
+    MBERT_PROFILE_LAYERNORM = 4,
+    MBERT_PROFILE_SLOTS = 5
 };
 
 /* Synchronise on the recorded events and return, per profile slot (index
- * MBERT_GLOBAL, MBERT_LOCAL or MBERT_PROFILE_OUT_PROJ of the host arrays
- * kernel_ms[3] and kernel_launches[3]), the summed kernel milliseconds and
+ * MBERT_GLOBAL, MBERT_LOCAL, MBERT_PROFILE_OUT_PROJ, MBERT_PROFILE_QKV_PROJ
+ * or MBERT_PROFILE_LAYERNORM of the host arrays kernel_ms[5] and
+ * kernel_launches[5]), the summed kernel milliseconds and
  * the number of recorded kernels, plus the number of kernels enqueued by
  * every entry point (*total_launches).  Clears all three.  Any output
  * pointer may be NULL. */
