@@ -45,7 +45,7 @@ N_SETS = 6
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # the ncu captures of the one-sequence 8192-token workload summarised in
-# profiles/attn_{global,local}_kernel_config3.md.  Reported only while the
+# profiles/*_kernel_config3.md.  Reported only while the
 # kernel sources still hash to what was captured.
 NCU_TRAFFIC = {
     "global": {"bytes": 39.64e6, "kernel": "attn_global_kernel",
@@ -53,7 +53,11 @@ NCU_TRAFFIC = {
     "local": {"bytes": 37.83e6, "kernel": "attn_local_kernel",
               "sources": {"attn_local.cu": "10494098048f75a4", "common.cuh": "c49de87f54892de8"}},
     "out_proj": {"bytes": 26.38e6, "kernel": "out_proj_kernel",
-                 "sources": {"out_proj.cu": "a90b9f6fda100937", "common.cuh": "c49de87f54892de8"}},
+                 "sources": {"projections.cu": "8da80e046fce28c7", "common.cuh": "c49de87f54892de8"}},
+    "qkv_proj": {"bytes": 16.20e6, "kernel": "qkv_proj_kernel",
+                 "sources": {"projections.cu": "8da80e046fce28c7", "common.cuh": "c49de87f54892de8"}},
+    "layernorm": {"bytes": 12.59e6, "kernel": "layernorm_kernel",
+                  "sources": {"layernorm.cu": "bb3e0cd506f60c79", "common.cuh": "c49de87f54892de8"}},
 }
 
 WORKLOADS = {
@@ -98,11 +102,12 @@ def load_peaks():
 
 def captured_traffic(kind, workload):
     """DRAM bytes per launch of a kernel ("global" / "local": the layer's
-    attention kernel; "out_proj": the projection), or None if the capture
-    does not apply (another workload, or the kernel source changed)."""
+    attention kernel; "out_proj", "qkv_proj", "layernorm": the projections
+    and the norm), or None if no capture applies (none taken, another
+    workload, or the kernel source changed since)."""
     import hashlib
-    rec = NCU_TRAFFIC[kind]
-    if workload != "config3":
+    rec = NCU_TRAFFIC.get(kind)
+    if rec is None or workload != "config3":
         return None
     csrc = os.path.join(ROOT, "encoder_only_transformer_gb300", "csrc")
     for name, digest in rec["sources"].items():
@@ -330,6 +335,32 @@ def run_ours(args):
     p_ms, p_n, _ = attn.profile_read()
     proj_ms = max_over_ranks(p_ms["out_proj"], world, dev) / max(1, p_n["out_proj"])
 
+    # --- the step before the block: qkv = LayerNorm(x) Wqkv^T on the same
+    # residual rows x (synthetic norm weight 1 + 0.1 N(0, 1), Wqkv ~
+    # N(0, 1/768)), timed alone: the norm kernel and the GEMM separately
+    gq = torch.Generator().manual_seed(4243)
+    norm_w = (1.0 + 0.1 * torch.randn(768, generator=gq)).to(torch.bfloat16).to(dev)
+    wqkv = (torch.randn(2304, 768, generator=gq) / 768 ** 0.5).to(torch.bfloat16).to(dev)
+    lnq_out = [torch.empty(T, 2304, dtype=torch.bfloat16, device=dev) for _ in range(N_SETS)]
+    for i in range(3):
+        attn.ln_qkv(x_sets[i % N_SETS], norm_w, wqkv, out=lnq_out[i % N_SETS])
+    attn.profile_read()
+    attn.profile(True)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    queue_ahead(kp)
+    a.record()
+    for i in range(kp):
+        attn.ln_qkv(x_sets[i % N_SETS], norm_w, wqkv, out=lnq_out[i % N_SETS])
+    b.record()
+    barrier()
+    attn.profile(False)
+    lnq_call_ms = max_over_ranks(a.elapsed_time(b), world, dev) / kp
+    p_ms, p_n, _ = attn.profile_read()
+    qkvp_ms = max_over_ranks(p_ms["qkv_proj"], world, dev) / max(1, p_n["qkv_proj"])
+    ln_ms = max_over_ranks(p_ms["layernorm"], world, dev) / max(1, p_n["layernorm"])
+    del lnq_out
+
     # --- end to end through the public API, pinned host buffers.  Every step
     # uploads both layers' qkv and reads both outputs back.  Copies and
     # compute are pipelined the way a serving loop would run them: uploads
@@ -421,6 +452,25 @@ def run_ours(args):
                         f"{kp} calls enqueued ahead of the GPU: kernel_ms from a CUDA event "
                         "pair around each launch, ms_per_call from one pair around all "
                         "calls; not part of the step"}
+    qf = 2.0 * T * 768 * 2304
+    qb = 2.0 * (T * 768 + T * 2304 + 2304 * 768)   # read h, write qkv, read Wqkv once
+    q_roof = max(qf / (peaks["bf16_tflops"] * 1e12), qb / (peaks["hbm_gbs"] * 1e9))
+    lb = 2.0 * (2 * T * 768 + 768)                 # read x, write h, read the weight
+    l_roof = lb / (peaks["hbm_gbs"] * 1e9)
+    ln_qkv = {
+        "ms_per_call": lnq_call_ms,
+        "qkv_proj": {"kernel": "qkv_proj_kernel", "kernel_ms": qkvp_ms,
+                     "tflops": qf / (qkvp_ms / 1e3) / 1e12, "hbm_gbs": qb / (qkvp_ms / 1e3) / 1e9,
+                     "bound": "tensor" if qf / (peaks["bf16_tflops"] * 1e12) >= qb / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                     "roofline_frac": q_roof / (qkvp_ms / 1e3), "gflop": qf / 1e9, "mbytes": qb / 1e6,
+                     "traffic": captured_traffic("qkv_proj", args.workload)},
+        "layernorm": {"kernel": "layernorm_kernel", "kernel_ms": ln_ms,
+                      "hbm_gbs": lb / (ln_ms / 1e3) / 1e9, "bound": "hbm",
+                      "roofline_frac": l_roof / (ln_ms / 1e3), "mbytes": lb / 1e6,
+                      "traffic": captured_traffic("layernorm", args.workload)},
+        "note": "qkv = LayerNorm(x) Wqkv^T from the residual rows x (the step before the "
+                f"block), timed alone over {kp} calls enqueued ahead of the GPU; kernel_ms "
+                "from a CUDA event pair around each launch; not part of the step"}
     g, lo = layers["global"], layers["local"]
     # The dominant kernel (the global layer's) against the tensor peak; the
     # local layer's kernel, HBM bound, against the copy bandwidth.  Kernel
@@ -455,6 +505,7 @@ def run_ours(args):
                    "parallelism": f"{world} independent replica(s), no collective"},
         "layers": layers,
         "out_proj": out_proj,
+        "ln_qkv": ln_qkv,
         "roofline": roofline,
         "roofline_local": roofline_local,
         "gpu_launches": launches,
