@@ -64,6 +64,11 @@ def lib():
         L.oracle_ln_qkv.argtypes = [u16p, u16p, u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_double, i64p, ctypes.c_int64, dp, ctypes.c_int]
         L.oracle_ln_qkv.restype = ctypes.c_int
+        L.oracle_gelu.argtypes = [dp, ctypes.c_int64, dp]
+        L.oracle_gelu.restype = None
+        L.oracle_mlp.argtypes = [u16p, u16p, u16p, u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_double, i64p, ctypes.c_int64, dp, ctypes.c_int]
+        L.oracle_mlp.restype = ctypes.c_int
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = ctypes.c_int
         _lib = L
@@ -249,6 +254,41 @@ def ln_qkv(x_bits, w_bits, wqkv_bits, eps: float = NORM_EPS, rows=None, threads:
     if rc:
         raise ValueError(f"oracle_ln_qkv failed (code {rc})")
     return out
+
+
+def gelu(z):
+    """The exact (erf) GELU, elementwise, fp64."""
+    zz = np.ascontiguousarray(z, dtype=np.float64)
+    out = np.empty_like(zz)
+    lib().oracle_gelu(_ptr(zz, ctypes.c_double), zz.size, _ptr(out, ctypes.c_double))
+    return out
+
+
+def mlp(x_bits, norm_w_bits, wi_bits, wo_bits, eps: float = NORM_EPS, rows=None, threads: int = 0):
+    """y = x + (GELU(g) * u) Wo^T, g, u = halves of LayerNorm(x) Wi^T, fp64.
+
+    x_bits: uint16 [T, d]; norm_w_bits: uint16 [d]; wi_bits: uint16
+    [2 * inner, d]; wo_bits: uint16 [d, inner] (bf16 bit patterns, weights
+    stored [out][in]).  Returns fp64 [n, d].
+    """
+    x = np.ascontiguousarray(x_bits)
+    w = np.ascontiguousarray(norm_w_bits)
+    wi = np.ascontiguousarray(wi_bits)
+    wo = np.ascontiguousarray(wo_bits)
+    for t in (x, w, wi, wo):
+        if t.dtype != np.uint16:
+            raise TypeError("inputs must be uint16 bf16 bit patterns")
+    T, d = x.shape
+    inner = wo.shape[1]
+    assert w.shape == (d,) and wi.shape == (2 * inner, d) and wo.shape == (d, inner)
+    n, r, rp = _rows_arg(rows, T)
+    y = np.empty((n, d), dtype=np.float64)
+    rc = lib().oracle_mlp(_ptr(x, ctypes.c_uint16), _ptr(w, ctypes.c_uint16),
+                          _ptr(wi, ctypes.c_uint16), _ptr(wo, ctypes.c_uint16), T, d, inner,
+                          float(eps), rp, n, _ptr(y, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError(f"oracle_mlp failed (code {rc})")
+    return y
 
 
 def attention_kind(qkv_bits, cu_seqlens, kind: str, rows=None, threads: int = 0):

@@ -583,6 +583,94 @@ int oracle_ln_qkv(const uint16_t *x, const uint16_t *w, const uint16_t *wqkv, in
     return bad ? -3 : 0;
 }
 
+/* ------------------------------------------------------------------ */
+/* the GeGLU MLP block                                                 */
+/* ------------------------------------------------------------------ */
+
+/* GELU in its exact form, z * Phi(z) = z / 2 * (1 + erf(z / sqrt 2)), not the
+ * tanh approximation ("ModernBERT" (candding), "The feed-forward halves": the
+ * activation is the exact erf GELU; "modernbert-base" (nest.franknoh), "Why
+ * the GELU matters"). */
+static double gelu_erf(double z)
+{
+    return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+}
+
+/* out[i] = gelu_erf(z[i]). */
+void oracle_gelu(const double *z, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = gelu_erf(z[i]);
+}
+
+/* y = x + (GELU(g) * u) Wo^T with g, u = the first and second halves of
+ * h Wi^T, h = LayerNorm(x; norm_w) ("ModernBERT-base Architecture
+ * Teardown", "What Does the GeGLU MLP Do?": Wi makes two vectors of 1152,
+ * the first goes through GELU, the second multiplies it number by number,
+ * Wo brings the 1152 back to 768; Wi [2 * inner][d] and Wo [d][inner] are
+ * Linear weights stored [out][in]; "modernbert-base" (nest.franknoh), "The
+ * fused projections": the first half of Wi's output is the GELU branch;
+ * "ModernBertModel" (safebydesign), "Implementing it": x = x + (gelu(g) * u)
+ * Wo^T after h = layernorm(x, mlp_norm)).  Every step in fp64, no
+ * intermediate rounding; y is fp64 [n][d]. */
+int oracle_mlp(const uint16_t *x, const uint16_t *norm_w, const uint16_t *wi, const uint16_t *wo,
+               int64_t T, int d, int inner, double eps, const int64_t *rows, int64_t n,
+               double *y, int threads)
+{
+    if (T < 0 || d <= 0 || inner <= 0 || n < 0 || eps < 0.0 || !norm_w)
+        return -1;
+    if (!rows)
+        n = T;
+    double *wim = malloc(sizeof(double) * 2 * (size_t)inner * (size_t)d);
+    double *wom = malloc(sizeof(double) * (size_t)d * (size_t)inner);
+    if (!wim || !wom) {
+        free(wim);
+        free(wom);
+        return -2;
+    }
+    for (int64_t e = 0; e < 2 * (int64_t)inner * d; e++)
+        wim[e] = bf16_to_f64(wi[e]);
+    for (int64_t e = 0; e < (int64_t)d * inner; e++)
+        wom[e] = bf16_to_f64(wo[e]);
+    int bad = 0;
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : oracle_max_threads()) reduction(|:bad)
+    for (int64_t k = 0; k < n; k++) {
+        const int64_t t = rows ? rows[k] : k;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        double *h = malloc(sizeof(double) * (size_t)d);
+        double *m = malloc(sizeof(double) * (size_t)inner);
+        if (!h || !m) {
+            free(h);
+            free(m);
+            bad = 1;
+            continue;
+        }
+        layernorm_row(x + t * d, norm_w, d, eps, h);
+        for (int j = 0; j < inner; j++) {
+            double g = 0.0, u = 0.0;
+            for (int c = 0; c < d; c++) {
+                g += h[c] * wim[(int64_t)j * d + c];
+                u += h[c] * wim[(int64_t)(inner + j) * d + c];
+            }
+            m[j] = gelu_erf(g) * u;
+        }
+        for (int o = 0; o < d; o++) {
+            double acc = 0.0;
+            for (int j = 0; j < inner; j++)
+                acc += m[j] * wom[(int64_t)o * inner + j];
+            y[k * d + o] = bf16_to_f64(x[t * d + o]) + acc;
+        }
+        free(h);
+        free(m);
+    }
+    free(wim);
+    free(wom);
+    return bad ? -3 : 0;
+}
+
 /* Number of OpenMP threads a parallel region would use by default. */
 int oracle_max_threads(void)
 {

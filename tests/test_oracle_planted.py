@@ -1,6 +1,6 @@
 """Planted mistakes: each plausible error, put into a copy of the oracle on
 the CPU, must make at least one pin (test_oracle.py, test_oracle_out_proj.py,
-test_oracle_ln_qkv.py) fail.
+test_oracle_ln_qkv.py, test_oracle_mlp.py) fail.
 
 The copy is made by a textual edit of the oracle's C source, compiled into a
 temporary library and swapped in for the duration of the check; the oracle
@@ -17,6 +17,7 @@ from oracle import build as obuild
 import test_oracle as T
 import test_oracle_out_proj as P
 import test_oracle_ln_qkv as N
+import test_oracle_mlp as M
 
 # (name, original source fragment, planted fragment)
 PLANTS = [
@@ -34,8 +35,8 @@ PLANTS = [
      "inv_freq[m] = pow(theta, -1.0 * (double)m / (double)head_dim);"),
     ("out_proj_transposed", "acc += ar[c] * w[(int64_t)o * d + c];",
      "acc += ar[c] * w[(int64_t)c * d + o];"),
-    ("out_proj_without_residual", "y[k * d + o] = bf16_to_f64(x[t * d + o]) + acc;",
-     "y[k * d + o] = acc;"),
+    ("out_proj_without_residual", "y[k * d + o] = bf16_to_f64(x[t * d + o]) + acc;\n        }\n        free(ar);",
+     "y[k * d + o] = acc;\n        }\n        free(ar);"),
     ("ln_unbiased_variance", "const double sd = sqrt(sq / d + eps);",
      "const double sd = sqrt(sq / (d - 1) + eps);"),
     ("ln_eps_outside_sqrt", "const double sd = sqrt(sq / d + eps);",
@@ -46,12 +47,17 @@ PLANTS = [
      "h[c] = (bf16_to_f64(x[c]) - mean) / sd;"),
     ("qkv_weight_transposed", "acc += h[c] * wm[(int64_t)j * d + c];",
      "acc += h[c] * wm[(int64_t)c * n_out + j];"),
+    ("gelu_tanh_form", "return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));",
+     "return 0.5 * z * (1.0 + tanh(sqrt(2.0 / 3.14159265358979323846) * (z + 0.044715 * z * z * z)));"),
+    ("mlp_halves_swapped", "m[j] = gelu_erf(g) * u;", "m[j] = gelu_erf(u) * g;"),
+    ("mlp_without_residual", "y[k * d + o] = bf16_to_f64(x[t * d + o]) + acc;\n        }\n        free(h);",
+     "y[k * d + o] = acc;\n        }\n        free(h);"),
 ]
 
 # every exported function whose ctypes signature the copies must share
 _FUNCS = ("oracle_inv_freq", "oracle_rope_row", "oracle_key_counts", "oracle_sdpa_dense",
           "oracle_attention", "oracle_out_proj", "oracle_layernorm", "oracle_ln_qkv",
-          "oracle_max_threads")
+          "oracle_gelu", "oracle_mlp", "oracle_max_threads")
 
 
 def _pins():
@@ -76,6 +82,9 @@ def _pins():
             N.test_shift_invariance_on_integers, N.test_weight_scales_positions,
             N.test_matches_torch_layer_norm, N.test_ln_qkv_equals_library_matmul,
             N.test_identity_norm_of_layer_zero, N.test_three_way_split_with_selection_weights]
+    out += [M.test_gelu_printed_values, M.test_gelu_matches_torch_exact_form,
+            M.test_zero_down_projection_returns_the_residual,
+            M.test_selection_weights_give_gelu_times_gate, M.test_matches_library_composition]
     out += [(lambda r=r: T.test_key_counts_match_pages(r)) for r in table]
     for lengths in ([5, 64, 65], [130, 7, 200]):
         for kind in ("global", "local"):
