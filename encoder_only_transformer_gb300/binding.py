@@ -20,6 +20,7 @@ _KINDS = {"global": GLOBAL, "local": LOCAL, GLOBAL: GLOBAL, LOCAL: LOCAL}
 
 HEADS, HEAD_DIM = 12, 64
 QKV_WIDTH, OUT_WIDTH = 3 * HEADS * HEAD_DIM, HEADS * HEAD_DIM
+MLP_INNER = 1152  # the GeGLU MLP's inner width (teardown, "What Does the GeGLU MLP Do?")
 NORM_EPS = 1e-5   # LayerNorm eps of ModernBERT-base (teardown, "What Does LayerNorm Do?")
 
 # Every symbol the public header declares, with its ctypes signature.
@@ -40,6 +41,7 @@ SIGNATURES = {
     "mbert_attn_key_counts": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp]),
     "mbert_attn_out_proj": (_c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _vp]),
     "mbert_attn_ln_qkv": (_c_int, [_vp, _vp, _vp, _vp, _c_i64, ctypes.c_float, _vp, _vp]),
+    "mbert_attn_mlp": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_i64, ctypes.c_float, _vp, _vp]),
     "mbert_attn_get_error": (_c_int, [_vp]),
     "mbert_attn_selftest_timeout": (_c_int, [_vp, _c_i64, _vp]),
     "mbert_attn_forward_noalloc": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp,
@@ -223,6 +225,29 @@ class Attention:
         _check(st, "ln_qkv")
         return out
 
+    def mlp(self, x: torch.Tensor, norm_w: torch.Tensor, wi: torch.Tensor, wo: torch.Tensor,
+            eps: float = NORM_EPS, out: torch.Tensor = None) -> torch.Tensor:
+        """y[T, 768] bf16 = x + (GELU(g) * u) Wo^T, g and u the halves of
+        LayerNorm(x) Wi^T (norm_w [768], Wi [2304, 768], Wo [768, 1152], stored
+        [out, in]).  `out` may be `x` itself."""
+        def check(t, name, shape):
+            if (t.dtype != torch.bfloat16 or tuple(t.shape) != shape or t.device != self.device
+                    or not t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous bf16 {list(shape)} tensor on {self.device}")
+        T = x.shape[0] if x.dim() == 2 else -1
+        check(x, "x", (T, OUT_WIDTH))
+        check(norm_w, "norm_w", (OUT_WIDTH,))
+        check(wi, "wi", (2 * MLP_INNER, OUT_WIDTH))
+        check(wo, "wo", (OUT_WIDTH, MLP_INNER))
+        if out is None:
+            out = torch.empty(T, OUT_WIDTH, dtype=torch.bfloat16, device=self.device)
+        check(out, "out", (T, OUT_WIDTH))
+        st = load_library().mbert_attn_mlp(self._h, x.data_ptr(), norm_w.data_ptr(), wi.data_ptr(),
+                                           wo.data_ptr(), T, float(eps), out.data_ptr(),
+                                           _stream_ptr(self.device))
+        _check(st, "mlp")
+        return out
+
     def key_counts(self, cu_seqlens: torch.Tensor, total_tokens: int, layer_kind,
                    max_seqlen: int = 0) -> torch.Tensor:
         """int32 [T]: keys the kernels' schedule and mask admit per query row."""
@@ -246,10 +271,10 @@ class Attention:
         _check(load_library().mbert_attn_profile_enable(self._h, 1 if enable else 0), "profile")
 
     def profile_read(self):
-        """-> ({'global': ms, 'local': ms, 'out_proj': ms, 'qkv_proj': ms,
-        'layernorm': ms}, the same keys -> kernel count, total_launches);
-        synchronises and clears the record."""
-        keys = ("global", "local", "out_proj", "qkv_proj", "layernorm")
+        """-> ({'global', 'local', 'out_proj', 'qkv_proj', 'layernorm', 'mlp_up',
+        'mlp_down'} -> summed kernel ms, the same keys -> kernel count,
+        total_launches); synchronises and clears the record."""
+        keys = ("global", "local", "out_proj", "qkv_proj", "layernorm", "mlp_up", "mlp_down")
         ms = (ctypes.c_double * len(keys))()
         n = (ctypes.c_int64 * len(keys))()
         tot = ctypes.c_int64()
@@ -291,6 +316,14 @@ def ln_qkv(x: torch.Tensor, norm_w, wqkv: torch.Tensor, eps: float = NORM_EPS,
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor")
     return _default(x.device).ln_qkv(x, norm_w, wqkv, eps, out)
+
+
+def mlp(x: torch.Tensor, norm_w: torch.Tensor, wi: torch.Tensor, wo: torch.Tensor,
+        eps: float = NORM_EPS, out: torch.Tensor = None) -> torch.Tensor:
+    """y = x + (GELU(g) * u) Wo^T after the MLP's LayerNorm (bf16, CUDA tensors)."""
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    return _default(x.device).mlp(x, norm_w, wi, wo, eps, out)
 
 
 def out_proj(a: torch.Tensor, wo: torch.Tensor, x: torch.Tensor, out: torch.Tensor = None) -> torch.Tensor:

@@ -20,6 +20,7 @@ constexpr int kHeadDim = 64;
 constexpr int kHidden = kHeads * kHeadDim;      // 768
 constexpr int kQKVWidth = 3 * kHidden;          // 2304
 constexpr int kPairs = kHeadDim / 2;            // 32 RoPE pairs per head
+constexpr int kInnerMlp = 1152;                 // the GeGLU MLP's inner width (Wi: 2 x 1152)
 
 constexpr int kBlockM = 128;                    // query rows per tile
 constexpr int kBlockN = 128;                    // key rows per tile

@@ -33,8 +33,10 @@ struct mbert_attn {
     int64_t work_cap = 0;                   // entries
     __nv_bfloat16 *rot = nullptr;           // rotated Q/K scratch [rows][1536]
     int64_t rot_cap = 0;                    // rows
-    __nv_bfloat16 *ln = nullptr;            // normalised rows [ln_cap][768] (ln_qkv)
+    __nv_bfloat16 *ln = nullptr;            // normalised rows [ln_cap][768] (ln_qkv, mlp)
     int64_t ln_cap = 0;                     // rows
+    __nv_bfloat16 *mid = nullptr;           // GELU(g) * u rows [mid_cap][1152] (mlp)
+    int64_t mid_cap = 0;                    // rows
     // global layers: split of the (entry, head, key tile) iterations among
     // one persistent CTA per SM
     int32_t *tile_start = nullptr;          // [entries + 1]
@@ -147,6 +149,7 @@ int grow_workspace(mbert_attn *h, int64_t entries, int64_t rot_rows)
             cudaDeviceSynchronize();
             cudaFree(h->rot);
         cudaFree(h->ln);
+        cudaFree(h->mid);
         }
         h->rot = r;
         h->rot_cap = cap;
@@ -156,6 +159,27 @@ int grow_workspace(mbert_attn *h, int64_t entries, int64_t rot_rows)
 
 // 2-D bf16 tensor map over [rows][width] (row pitch = width * 2 bytes),
 // box 64 columns x 128 rows, 128-byte swizzle, out-of-range reads give 0.
+// Grow a handle-owned bf16 buffer of `width` columns to at least `rows` rows
+// (at least 8192); the old buffer is freed after the device is idle.
+int grow_rows(__nv_bfloat16 **buf, int64_t *cap, int64_t rows, int width)
+{
+    if (rows <= *cap)
+        return MBERT_OK;
+    const int64_t n = rows < 8192 ? 8192 : rows;
+    __nv_bfloat16 *p = nullptr;
+    if (cudaMalloc(&p, sizeof(__nv_bfloat16) * static_cast<size_t>(width) * n) != cudaSuccess) {
+        cudaGetLastError();
+        return MBERT_ERR_OOM;
+    }
+    if (*buf) {
+        cudaDeviceSynchronize();
+        cudaFree(*buf);
+    }
+    *buf = p;
+    *cap = n;
+    return MBERT_OK;
+}
+
 // The next event pair of a profile slot (both null while profiling is off).
 int profile_events(mbert_attn *h, int slot, cudaEvent_t *ev0, cudaEvent_t *ev1)
 {
@@ -605,20 +629,9 @@ MBERT_API int mbert_attn_ln_qkv(mbert_attn *h, const void *x, const void *norm_w
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const void *a = x;
     if (norm_w) {
-        if (T > h->ln_cap) {
-            const int64_t cap = T < 8192 ? 8192 : T;
-            __nv_bfloat16 *buf = nullptr;
-            if (cudaMalloc(&buf, sizeof(__nv_bfloat16) * kHidden * cap) != cudaSuccess) {
-                cudaGetLastError();
-                return MBERT_ERR_OOM;
-            }
-            if (h->ln) {
-                cudaDeviceSynchronize();
-                cudaFree(h->ln);
-            }
-            h->ln = buf;
-            h->ln_cap = cap;
-        }
+        const int rc = grow_rows(&h->ln, &h->ln_cap, T, kHidden);
+        if (rc != MBERT_OK)
+            return rc;
         a = h->ln;
     }
     QkvProjArgs q;
@@ -654,6 +667,75 @@ MBERT_API int mbert_attn_ln_qkv(mbert_attn *h, const void *x, const void *norm_w
     if (e == cudaSuccess && ev1)
         e = cudaEventRecord(ev1, st);
     h->launches += 1;
+    h->last_stream = st;
+    return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
+}
+
+MBERT_API int mbert_attn_mlp(mbert_attn *h, const void *x, const void *norm_w, const void *wi,
+                             const void *wo, int64_t total_tokens, float eps, void *y, void *stream)
+{
+    if (!h || total_tokens < 0 || total_tokens > INT32_MAX || !(eps >= 0.f) || eps > 1.f)
+        return MBERT_ERR_BAD_ARG;
+    const int64_t T = total_tokens;
+    if (T == 0)
+        return MBERT_OK;
+    if (!x || !norm_w || !wi || !wo || !y)
+        return MBERT_ERR_BAD_ARG;
+    for (const void *ptr : {x, norm_w, wi, wo, static_cast<const void *>(y)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15)
+            return MBERT_ERR_BAD_ARG;
+    const size_t act = static_cast<size_t>(T) * kHidden * 2;
+    const size_t wib = static_cast<size_t>(2 * kInnerMlp) * kHidden * 2;
+    const size_t wob = static_cast<size_t>(kHidden) * kInnerMlp * 2;
+    if (ranges_overlap(wi, wib, y, act) || ranges_overlap(wo, wob, y, act) ||
+        ranges_overlap(norm_w, kHidden * 2, y, act) || (x != y && ranges_overlap(x, act, y, act)))
+        return MBERT_ERR_BAD_ARG;
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = grow_rows(&h->ln, &h->ln_cap, T, kHidden);
+    if (rc == MBERT_OK)
+        rc = grow_rows(&h->mid, &h->mid_cap, T, kInnerMlp);
+    if (rc != MBERT_OK)
+        return rc;
+    QkvProjArgs up;
+    OutProjArgs down;
+    if (encode_map(h, &up.tm_a, h->ln, kHidden, T) != MBERT_OK ||
+        encode_map(h, &up.tm_w, wi, kHidden, 2 * kInnerMlp) != MBERT_OK ||
+        encode_map(h, &up.tm_y, h->mid, kInnerMlp, T) != MBERT_OK ||
+        encode_map(h, &down.tm_a, h->mid, kInnerMlp, T) != MBERT_OK ||
+        encode_map(h, &down.tm_w, wo, kInnerMlp, kHidden) != MBERT_OK ||
+        encode_map(h, &down.tm_x, x, kHidden, T) != MBERT_OK ||
+        encode_map(h, &down.tm_y, y, kHidden, T) != MBERT_OK)
+        return MBERT_ERR_CUDA;
+    up.T = down.T = T;
+    up.num_ctas = down.num_ctas = h->num_sms;
+    up.err = down.err = h->err;
+    down.x = static_cast<const __nv_bfloat16 *>(x);
+    cudaError_t e = cudaSuccess;
+    // one event pair per kernel while profiling
+    auto timed = [&](int slot, auto &&launch) {
+        cudaEvent_t e0, e1;
+        if (e != cudaSuccess)
+            return;
+        if (profile_events(h, slot, &e0, &e1) != MBERT_OK) {
+            e = cudaErrorMemoryAllocation;
+            return;
+        }
+        if (e0)
+            e = cudaEventRecord(e0, st);
+        if (e == cudaSuccess)
+            e = launch();
+        if (e == cudaSuccess && e1)
+            e = cudaEventRecord(e1, st);
+        h->launches += 1;
+    };
+    timed(MBERT_PROFILE_LAYERNORM, [&] {
+        return launch_layernorm(static_cast<const __nv_bfloat16 *>(x),
+                                static_cast<const __nv_bfloat16 *>(norm_w), T, eps, h->ln,
+                                h->num_sms, st);
+    });
+    timed(MBERT_PROFILE_MLP_UP, [&] { return launch_mlp_up(up, st); });
+    timed(MBERT_PROFILE_MLP_DOWN, [&] { return launch_mlp_down(down, st); });
     h->last_stream = st;
     return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
 }

@@ -126,6 +126,13 @@ struct QkvProjArgs {
 
 cudaError_t launch_qkv_proj(const QkvProjArgs &a, cudaStream_t stream);
 
+// The GeGLU MLP's two GEMMs, on the same paired body: m = GELU(g) * u from
+// h [T][768] and Wi [2304][768] into m [T][1152] (tm_a over h with width
+// 768, tm_w over Wi, tm_y over m), then y = x + m Wo^T with Wo [768][1152]
+// (tm_a over m and tm_w over Wo, both width 1152).
+cudaError_t launch_mlp_up(const QkvProjArgs &a, cudaStream_t stream);
+cudaError_t launch_mlp_down(const OutProjArgs &a, cudaStream_t stream);
+
 // Bias-free LayerNorm of each row of x [T][768] (bf16) with weight w [768]
 // into h [T][768] (bf16): one warp per row, fp32 statistics.
 cudaError_t launch_layernorm(const __nv_bfloat16 *x, const __nv_bfloat16 *w, long long T,

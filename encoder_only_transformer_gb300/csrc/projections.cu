@@ -10,7 +10,14 @@
 //    [T][768], Wo bf16 [768][768] stored [out][in] (same section: Wo maps
 //    the joined heads back from 768 to 768), x the residual stream bf16
 //    [T][768] ("Implementing it": x = x + a Wo^T); y bf16 [T][768].
-// Both accumulate in fp32 and round once to bf16; K = 768.
+//  * mlp_up_kernel: m = GELU(g) * u with g, u the first and second halves of
+//    h Wi^T, h bf16 [T][768] (the MLP's LayerNorm output), Wi bf16
+//    [2304][768] ("ModernBERT-base Architecture Teardown", "What Does the
+//    GeGLU MLP Do?"; the first half is the GELU branch, "modernbert-base",
+//    "The fused projections"), GELU in the exact erf form ("ModernBERT"
+//    (candding), "The feed-forward halves"); m bf16 [T][1152].
+//  * mlp_down_kernel: y = x + m Wo^T, Wo bf16 [768][1152] (K = 1152).
+// All accumulate in fp32 and round once to bf16.
 //
 // The tensor pipe of one SM takes 128 x N x 16 per 64 clocks at N = 128,
 // and an SM's copy engine delivers about 64 bytes per clock, which feeds a
@@ -46,12 +53,11 @@ namespace {
 
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
-constexpr int kD = kHidden;             // 768
 constexpr int kBM = 128;                // rows per CTA
 constexpr int kUnitM = 2 * kBM;         // rows per unit (the pair)
 constexpr int kBN = 256;                // output columns per unit (MMA N)
 constexpr int kBK = 64;
-constexpr int kKSteps = kD / kBK;       // 12
+constexpr int kInner = kInnerMlp;       // the MLP's inner width
 constexpr int kStages = 5;
 constexpr uint32_t kStageBytes = 2 * kTileBytes;             // A box + B box (this CTA's half)
 constexpr uint32_t kOffRing = 0;
@@ -196,9 +202,45 @@ __device__ __forceinline__ void store_row(uint32_t rowp, int r, const uint32_t (
     }
 }
 
-// The kernel body: output columns in kColBlocks blocks of 256; with
-// kResidual, y = x + D, else y = D.
-template <int kColBlocks, bool kResidual>
+// What the epilogue makes of the accumulator D of a unit.
+enum class Epi {
+    kPlain,      // y = D (256 output columns per unit)
+    kResidual,   // y = x + D (256 output columns per unit)
+    kGeglu       // y = GELU(g) * u (128 output columns per unit; D holds g, then u)
+};
+
+// GELU(g) * u for 64 output columns of one row into the swizzled staging
+// row, GELU in its exact erf form: z / 2 * (1 + erf(z / sqrt 2)).
+__device__ __forceinline__ void geglu_row(uint32_t rowp, int r, const uint32_t (&g)[2][32],
+                                          const uint32_t (&u)[2][32])
+{
+    constexpr float kRsqrt2 = 0.70710678118654752f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint32_t yw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float m[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int col = 8 * (c % 4) + 2 * e + k;
+                const float z = __uint_as_float(g[c / 4][col]);
+                m[k] = 0.5f * z * (1.0f + erff(z * kRsqrt2)) * __uint_as_float(u[c / 4][col]);
+            }
+            yw[e] = pack_bf16x2(m[0], m[1]);
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
+                     :: "r"(rowp + ((c ^ (r & 7)) << 4)), "r"(yw[0]), "r"(yw[1]), "r"(yw[2]), "r"(yw[3])
+                     : "memory");
+    }
+}
+
+// The kernel body: K = 64 kKSteps; kColBlocks column blocks per row block of
+// 256 rows.  kPlain / kResidual: block j is output columns 256 j .. + 255,
+// weight rows the same.  kGeglu: block j is output columns 128 j .. + 127,
+// from weight rows 128 j .. + 127 (g, the leader CTA's half of B) and
+// kInner + 128 j .. + 127 (u, the peer's half).
+template <int kKSteps, int kColBlocks, Epi kEpi>
 __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtensorMap &tm_w,
                                           const CUtensorMap &tm_x, const CUtensorMap &tm_y,
                                           const __nv_bfloat16 *x, long long T, int n_units,
@@ -225,7 +267,7 @@ __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtenso
     } else if (tid == 0) {
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_w);
-        if constexpr (kResidual)
+        if constexpr (kEpi == Epi::kResidual)
             tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_y);
         for (int i = 0; i < kNumBars; ++i) {
@@ -257,7 +299,8 @@ __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtenso
         for (int i = 0; i < my_units && ok; ++i) {
             const int u = u_begin + i;
             const int m0 = (u / kColBlocks) * kUnitM + rank * kBM;
-            const int w0 = (u % kColBlocks) * kBN + rank * (kBN / 2);
+            const int w0 = kEpi == Epi::kGeglu ? rank * kInner + (u % kColBlocks) * (kBN / 2)
+                                               : (u % kColBlocks) * kBN + rank * (kBN / 2);
             for (int k = 0; k < kKSteps && ok; ++k, ++g) {
                 const int st = g % kStages;
                 if (!(ok = mbar_wait(barp(base, kBarEmpty + st), ((g / kStages) & 1) ^ 1u, err)))
@@ -312,19 +355,23 @@ __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtenso
         }
     } else {
         // ------------------------------------------------------ epilogue
+        constexpr bool kRes = kEpi == Epi::kResidual;
+        constexpr int kOutCols = kEpi == Epi::kGeglu ? kBN / 2 : kBN;   // output columns per unit
+        constexpr int kOutBoxes = kOutCols / 64;
+        constexpr int kOutWidth = kColBlocks * kOutCols;               // row length of y (and x)
         const int q = warp & 3;                        // TMEM lane quadrant: rows 32 q .. 32 q + 31
-        const int hf = (warp - 2) >> 2;                // column half: boxes 2 hf, 2 hf + 1
+        const int hf = (warp - 2) >> 2;                // column half of the unit's output
         const int r = 32 * q + lane;                   // row in the tile, TMEM lane
         const bool lead = warp == 2 && lane == 0;      // x loads and y stores
         const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
         const uint64_t once = l2_policy_evict_first(); // x: read once
         auto unit_m0 = [&](int i) { return ((u_begin + i) / kColBlocks) * kUnitM + rank * kBM; };
-        auto unit_n0 = [&](int i) { return ((u_begin + i) % kColBlocks) * kBN; };
+        auto unit_n0 = [&](int i) { return ((u_begin + i) % kColBlocks) * kOutCols; };
         // this thread's half row of unit i's x into L2
         auto prefetch_x = [&](int i) {
             const long long row = static_cast<long long>(unit_m0(i)) + r;
             if (row < T)
-                l2_prefetch_bytes(x + static_cast<size_t>(row) * (kColBlocks * kBN) + unit_n0(i) + 128 * hf, 256);
+                l2_prefetch_bytes(x + static_cast<size_t>(row) * kOutWidth + unit_n0(i) + 128 * hf, 256);
         };
         auto load_x = [&](int i) {                     // unit i's x into the staging tile
             const uint32_t bar = barp(base, kBarXFull);
@@ -333,7 +380,7 @@ __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtenso
                 tma_load_2d_hint(base + kOffY + b * kTileBytes, &tm_x, unit_n0(i) + 64 * b, unit_m0(i), bar, once);
         };
         int x_issued = 0, x_done = 0;
-        if constexpr (kResidual) {
+        if constexpr (kRes) {
             if (lead && my_units > 0) {
                 load_x(0);
                 x_issued = 1;
@@ -341,7 +388,7 @@ __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtenso
         }
         bool ok = true;
         for (int i = 0; i < my_units && ok; ++i) {
-            if constexpr (kResidual) {
+            if constexpr (kRes) {
                 if (i + 1 < my_units)
                     prefetch_x(i + 1);                 // a unit ahead of its load
             }
@@ -349,7 +396,7 @@ __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtenso
             // the accumulator is complete; with the residual the unit's x has
             // landed, otherwise the previous unit's store has read the tile
             bool ready = mbar_wait(barp(base, kBarAccFull + acc), static_cast<uint32_t>(i >> 1) & 1u, err);
-            if constexpr (kResidual)
+            if constexpr (kRes)
                 ready = ready && mbar_wait(barp(base, kBarXFull), static_cast<uint32_t>(i & 1), err);
             else
                 ready = ready && (i == 0 || mbar_wait(barp(base, kBarXFull), static_cast<uint32_t>((i - 1) & 1), err));
@@ -358,27 +405,44 @@ __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtenso
             x_done = i + 1;
             __syncwarp();
             tc_fence_after();
-            // box 2 hf + bb holds columns 64 (2 hf + bb) .. + 63; the second
-            // box's accumulator loads while the first is written
-            uint32_t va[2][32], vb[2][32];
-            tmem_ld32(tmem + acc * kBN + lane_off + 128 * hf, va[0]);
-            tmem_ld32(tmem + acc * kBN + lane_off + 128 * hf + 32, va[1]);
-            tmem_wait_ld();
-            reg_fence32(va[0]);
-            reg_fence32(va[1]);
-            tmem_ld32(tmem + acc * kBN + lane_off + 128 * hf + 64, vb[0]);
-            tmem_ld32(tmem + acc * kBN + lane_off + 128 * hf + 96, vb[1]);
-            if constexpr (kResidual)
-                add_x_row(base + kOffY + (2 * hf) * kTileBytes + r * 128, r, va);
-            else
-                store_row(base + kOffY + (2 * hf) * kTileBytes + r * 128, r, va);
-            tmem_wait_ld();
-            reg_fence32(vb[0]);
-            reg_fence32(vb[1]);
-            if constexpr (kResidual)
-                add_x_row(base + kOffY + (2 * hf + 1) * kTileBytes + r * 128, r, vb);
-            else
-                store_row(base + kOffY + (2 * hf + 1) * kTileBytes + r * 128, r, vb);
+            const uint32_t dacc = tmem + acc * kBN + lane_off;
+            if constexpr (kEpi == Epi::kGeglu) {
+                // output columns 64 hf .. + 63: g at accumulator columns
+                // 64 hf .., u at 128 + 64 hf ..
+                uint32_t vg[2][32], vu[2][32];
+                tmem_ld32(dacc + 64 * hf, vg[0]);
+                tmem_ld32(dacc + 64 * hf + 32, vg[1]);
+                tmem_ld32(dacc + 128 + 64 * hf, vu[0]);
+                tmem_ld32(dacc + 128 + 64 * hf + 32, vu[1]);
+                tmem_wait_ld();
+                reg_fence32(vg[0]);
+                reg_fence32(vg[1]);
+                reg_fence32(vu[0]);
+                reg_fence32(vu[1]);
+                geglu_row(base + kOffY + hf * kTileBytes + r * 128, r, vg, vu);
+            } else {
+                // box 2 hf + bb holds columns 64 (2 hf + bb) .. + 63; the
+                // second box's accumulator loads while the first is written
+                uint32_t va[2][32], vb[2][32];
+                tmem_ld32(dacc + 128 * hf, va[0]);
+                tmem_ld32(dacc + 128 * hf + 32, va[1]);
+                tmem_wait_ld();
+                reg_fence32(va[0]);
+                reg_fence32(va[1]);
+                tmem_ld32(dacc + 128 * hf + 64, vb[0]);
+                tmem_ld32(dacc + 128 * hf + 96, vb[1]);
+                if constexpr (kRes)
+                    add_x_row(base + kOffY + (2 * hf) * kTileBytes + r * 128, r, va);
+                else
+                    store_row(base + kOffY + (2 * hf) * kTileBytes + r * 128, r, va);
+                tmem_wait_ld();
+                reg_fence32(vb[0]);
+                reg_fence32(vb[1]);
+                if constexpr (kRes)
+                    add_x_row(base + kOffY + (2 * hf + 1) * kTileBytes + r * 128, r, vb);
+                else
+                    store_row(base + kOffY + (2 * hf + 1) * kTileBytes + r * 128, r, vb);
+            }
             // the accumulator may be reused: one arrival per warp at the leader
             tc_fence_before();
             __syncwarp();
@@ -391,11 +455,11 @@ __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtenso
                     break;
                 const int m0 = unit_m0(i);
                 if (m0 < T) {                            // rows past T are not stored
-                    for (int b = 0; b < kYBoxes; ++b)
+                    for (int b = 0; b < kOutBoxes; ++b)
                         tma_store_2d(&tm_y, base + kOffY + b * kTileBytes, unit_n0(i) + 64 * b, m0);
                     bulk_commit();
                 }
-                if constexpr (kResidual) {
+                if constexpr (kRes) {
                     if (i + 1 < my_units) {
                         bulk_wait_read0();               // the store has read the staging tile
                         load_x(i + 1);
@@ -409,7 +473,7 @@ __device__ __forceinline__ void pair_gemm(const CUtensorMap &tm_a, const CUtenso
         }
         if (lead) {
             // an x load still in flight after a timeout lands before the exit
-            if (kResidual && x_done < x_issued)
+            if (kRes && x_done < x_issued)
                 mbar_wait(barp(base, kBarXFull), static_cast<uint32_t>((x_issued - 1) & 1), err, kDrainLimitNs);
             bulk_wait0();                                // the stores have completed
         }
@@ -428,14 +492,32 @@ out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                 const __nv_bfloat16 *x, long long T, int n_units, int32_t *err)
 {
-    pair_gemm<kHidden / kBN, true>(tm_a, tm_w, tm_x, tm_y, x, T, n_units, err);
+    pair_gemm<kHidden / kBK, kHidden / kBN, Epi::kResidual>(tm_a, tm_w, tm_x, tm_y, x, T, n_units, err);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_y, long long T, int n_units, int32_t *err)
 {
-    pair_gemm<kQKVWidth / kBN, false>(tm_a, tm_w, tm_y, tm_y, nullptr, T, n_units, err);
+    pair_gemm<kHidden / kBK, kQKVWidth / kBN, Epi::kPlain>(tm_a, tm_w, tm_y, tm_y, nullptr, T, n_units, err);
+}
+
+// The MLP's first GEMM with its GeGLU: m = GELU(h Wi_g^T) * (h Wi_u^T),
+// [T][1152] from h [T][768] and Wi [2304][768].
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mlp_up_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+              const __grid_constant__ CUtensorMap tm_y, long long T, int n_units, int32_t *err)
+{
+    pair_gemm<kHidden / kBK, kInner / (kBN / 2), Epi::kGeglu>(tm_a, tm_w, tm_y, tm_y, nullptr, T, n_units, err);
+}
+
+// The MLP's second GEMM with the residual: y = x + m Wo^T, K = 1152.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mlp_down_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+                const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+                const __nv_bfloat16 *x, long long T, int n_units, int32_t *err)
+{
+    pair_gemm<kInner / kBK, kHidden / kBN, Epi::kResidual>(tm_a, tm_w, tm_x, tm_y, x, T, n_units, err);
 }
 
 // Pairs of CTAs to launch for `kernel`: as many as fit at once (per device,
@@ -483,6 +565,21 @@ cudaError_t launch_out_proj(const OutProjArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+cudaError_t launch_mlp_down(const OutProjArgs &a, cudaStream_t stream)
+{
+    static int max_pairs[64] = {};
+    const long long n_units = ((a.T + kUnitM - 1) / kUnitM) * (kHidden / kBN);
+    if (n_units <= 0)
+        return cudaSuccess;
+    int pairs = 0;
+    cudaError_t e = pair_count(mlp_down_kernel, max_pairs, a.num_ctas, n_units, &pairs);
+    if (e != cudaSuccess)
+        return e;
+    mlp_down_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(
+        a.tm_a, a.tm_w, a.tm_x, a.tm_y, a.x, a.T, static_cast<int>(n_units), a.err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_qkv_proj(const QkvProjArgs &a, cudaStream_t stream)
 {
     static int max_pairs[64] = {};
@@ -494,6 +591,21 @@ cudaError_t launch_qkv_proj(const QkvProjArgs &a, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     qkv_proj_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(
+        a.tm_a, a.tm_w, a.tm_y, a.T, static_cast<int>(n_units), a.err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mlp_up(const QkvProjArgs &a, cudaStream_t stream)
+{
+    static int max_pairs[64] = {};
+    const long long n_units = ((a.T + kUnitM - 1) / kUnitM) * (kInner / (kBN / 2));
+    if (n_units <= 0)
+        return cudaSuccess;
+    int pairs = 0;
+    cudaError_t e = pair_count(mlp_up_kernel, max_pairs, a.num_ctas, n_units, &pairs);
+    if (e != cudaSuccess)
+        return e;
+    mlp_up_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(
         a.tm_a, a.tm_w, a.tm_y, a.T, static_cast<int>(n_units), a.err);
     return cudaGetLastError();
 }

@@ -148,6 +148,32 @@ int mbert_attn_key_counts(mbert_attn *h, const int32_t *cu_seqlens, int n_seqs,
 int mbert_attn_ln_qkv(mbert_attn *h, const void *x, const void *norm_w, const void *wqkv,
                       int64_t total_tokens, float eps, void *qkv, void *stream);
 
+/* The layer's second block, the GeGLU MLP with its pre-norm and residual:
+ * y = x + (GELU(g) * u) Wo^T with g, u the first and second halves of
+ * LayerNorm(x) Wi^T ("ModernBERT-base Architecture Teardown", "What Does
+ * the GeGLU MLP Do?": Wi makes two vectors of 1152, the first goes through
+ * GELU and the second multiplies it, Wo brings 1152 back to 768;
+ * "modernbert-base" (nest.franknoh), "The fused projections": the first
+ * half of Wi's output is the GELU branch).  GELU is the exact erf form
+ * ("ModernBERT" (candding), "The feed-forward halves"); the LayerNorm is as
+ * in mbert_attn_ln_qkv.
+ *   x       device bf16 [total_tokens][768]: the residual stream.
+ *   norm_w  device bf16 [768]: the MLP norm's weight (not NULL).
+ *   wi      device bf16 [2304][768], [out][in].
+ *   wo      device bf16 [768][1152], [out][in].
+ *   eps     as in mbert_attn_ln_qkv.
+ *   y       device bf16 [total_tokens][768]: written.  y may be x itself
+ *           (in-place update); it must not overlap the weights, and must
+ *           overlap x either exactly or not at all.
+ * Three kernels: the norm (fp32, bf16 result), Wi with the GeGLU in its
+ * epilogue (fp32 accumulation, GELU(g) * u rounded to bf16), Wo with the
+ * residual (fp32, y rounded to bf16 once).  The norm's output and the
+ * [total_tokens][1152] intermediate live in handle-owned buffers (grown
+ * with cudaMalloc when needed); calls sharing a handle must not overlap on
+ * the GPU.  All pointers 16-byte aligned.  Returns as mbert_attn_ln_qkv. */
+int mbert_attn_mlp(mbert_attn *h, const void *x, const void *norm_w, const void *wi,
+                   const void *wo, int64_t total_tokens, float eps, void *y, void *stream);
+
 /* The step after the attention block: the output projection with the
  * residual add, y = x + a Wo^T ("ModernBERT-base Architecture Teardown",
  * "How Does ModernBERT Make Q, K and V?": Wo maps the joined heads back from
@@ -213,23 +239,26 @@ int mbert_attn_forward_noalloc(const void *qkv, const int32_t *cu_seqlens, int n
 /* Measurement.  While enabled, every mbert_attn_forward also records a
  * CUDA event pair on its stream around its attention kernel (the plan and
  * RoPE kernels before it are outside the pair), every mbert_attn_out_proj
- * one around its kernel, and every mbert_attn_ln_qkv one around each of its
- * two kernels.  The handle always counts the kernels it enqueues. */
+ * one around its kernel, and every mbert_attn_ln_qkv and mbert_attn_mlp one
+ * around each of their kernels.  The handle always counts the kernels it enqueues. */
 int mbert_attn_profile_enable(mbert_attn *h, int enable);
 
 /* Profile slots: the two layer kinds, the output projection, the Wqkv
- * projection and the pre-attention LayerNorm. */
+ * projection, the LayerNorm (before attention or before the MLP) and the
+ * MLP's two GEMMs. */
 enum {
     MBERT_PROFILE_OUT_PROJ = 2,
     MBERT_PROFILE_QKV_PROJ = 3,
     MBERT_PROFILE_LAYERNORM = 4,
-    MBERT_PROFILE_SLOTS = 5
+    MBERT_PROFILE_MLP_UP = 5,
+    MBERT_PROFILE_MLP_DOWN = 6,
+    MBERT_PROFILE_SLOTS = 7
 };
 
 /* Synchronise on the recorded events and return, per profile slot (index
- * MBERT_GLOBAL, MBERT_LOCAL, MBERT_PROFILE_OUT_PROJ, MBERT_PROFILE_QKV_PROJ
- * or MBERT_PROFILE_LAYERNORM of the host arrays kernel_ms[5] and
- * kernel_launches[5]), the summed kernel milliseconds and
+ * MBERT_GLOBAL, MBERT_LOCAL or MBERT_PROFILE_* of the host arrays
+ * kernel_ms[MBERT_PROFILE_SLOTS] and kernel_launches[MBERT_PROFILE_SLOTS]),
+ * the summed kernel milliseconds and
  * the number of recorded kernels, plus the number of kernels enqueued by
  * every entry point (*total_launches).  Clears all three.  Any output
  * pointer may be NULL. */
