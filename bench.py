@@ -361,6 +361,60 @@ def run_ours(args):
     ln_ms = max_over_ranks(p_ms["layernorm"], world, dev) / max(1, p_n["layernorm"])
     del lnq_out
 
+    # --- the layer's second block: y = x + MLP(LayerNorm(x)) on the residual
+    # rows (synthetic norm weight 1 + 0.1 N(0, 1), Wi ~ N(0, 1/768), Wo ~
+    # N(0, 1/1152)), timed alone: its three kernels separately
+    gm = torch.Generator().manual_seed(4244)
+    mlp_w = (1.0 + 0.1 * torch.randn(768, generator=gm)).to(torch.bfloat16).to(dev)
+    mlp_wi = (torch.randn(2304, 768, generator=gm) / 768 ** 0.5).to(torch.bfloat16).to(dev)
+    mlp_wo = (torch.randn(768, 1152, generator=gm) / 1152 ** 0.5).to(torch.bfloat16).to(dev)
+    for i in range(3):
+        attn.mlp(x_sets[i % N_SETS], mlp_w, mlp_wi, mlp_wo, out=y_sets[i % N_SETS])
+    attn.profile_read()
+    attn.profile(True)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    queue_ahead(kp)
+    a.record()
+    for i in range(kp):
+        attn.mlp(x_sets[i % N_SETS], mlp_w, mlp_wi, mlp_wo, out=y_sets[i % N_SETS])
+    b.record()
+    barrier()
+    attn.profile(False)
+    mlp_call_ms = max_over_ranks(a.elapsed_time(b), world, dev) / kp
+    p_ms, p_n, _ = attn.profile_read()
+    mlp_ms = {k: max_over_ranks(p_ms[k], world, dev) / max(1, p_n[k])
+              for k in ("layernorm", "mlp_up", "mlp_down")}
+
+    # --- a whole encoder layer of each kind from the library's calls:
+    # qkv = LN(x) Wqkv^T, attention, x1 = x + a Wo^T, y = x1 + MLP(x1), on
+    # the step's packing; one event pair around each run of layers
+    lay_qkv = torch.empty(T, 2304, dtype=torch.bfloat16, device=dev)
+    lay_a = torch.empty(T, 768, dtype=torch.bfloat16, device=dev)
+    lay_x1 = torch.empty(T, 768, dtype=torch.bfloat16, device=dev)
+
+    def layer(i, kind):
+        x_in = x_sets[i % N_SETS]
+        attn.ln_qkv(x_in, norm_w, wqkv, out=lay_qkv)
+        attn.forward(lay_qkv, cu, kind, max_seqlen=L, out=lay_a)
+        attn.out_proj(lay_a, wo, x_in, out=lay_x1)
+        attn.mlp(lay_x1, mlp_w, mlp_wi, mlp_wo, out=y_sets[i % N_SETS])
+
+    layer_ms = {}
+    for kind in ("global", "local"):
+        for i in range(3):
+            layer(i, kind)
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        queue_ahead(4 * kk)
+        a.record()
+        for i in range(kk):
+            layer(i, kind)
+        b.record()
+        barrier()
+        layer_ms[kind] = max_over_ranks(a.elapsed_time(b), world, dev) / kk
+    del lay_qkv, lay_a, lay_x1
+
     # --- end to end through the public API, pinned host buffers.  Every step
     # uploads both layers' qkv and reads both outputs back.  Copies and
     # compute are pipelined the way a serving loop would run them: uploads
@@ -471,6 +525,34 @@ def run_ours(args):
         "note": "qkv = LayerNorm(x) Wqkv^T from the residual rows x (the step before the "
                 f"block), timed alone over {kp} calls enqueued ahead of the GPU; kernel_ms "
                 "from a CUDA event pair around each launch; not part of the step"}
+    uf, df = 2.0 * T * 768 * 2304, 2.0 * T * 1152 * 768
+    ub = 2.0 * (T * 768 + T * 1152 + 2304 * 768)          # read h, write GELU(g) * u, read Wi
+    db = 2.0 * (T * 1152 + 2 * T * 768 + 768 * 1152)      # read it and x, write y, read Wo
+
+    def gemm_rec(kernel, flops, nbytes, ms):
+        t = ms / 1e3
+        roof = max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+        return {"kernel": kernel, "kernel_ms": ms, "tflops": flops / t / 1e12,
+                "hbm_gbs": nbytes / t / 1e9,
+                "bound": "tensor" if flops / (peaks["bf16_tflops"] * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                "roofline_frac": roof / t, "gflop": flops / 1e9, "mbytes": nbytes / 1e6}
+    mlp = {"ms_per_call": mlp_call_ms,
+           "layernorm": {"kernel": "layernorm_kernel", "kernel_ms": mlp_ms["layernorm"],
+                         "hbm_gbs": lb / (mlp_ms["layernorm"] / 1e3) / 1e9,
+                         "roofline_frac": l_roof / (mlp_ms["layernorm"] / 1e3)},
+           "mlp_up": gemm_rec("mlp_up_kernel", uf, ub, mlp_ms["mlp_up"]),
+           "mlp_down": gemm_rec("mlp_down_kernel", df, db, mlp_ms["mlp_down"]),
+           "note": "y = x + (GELU(g) * u) Wo^T after the MLP's LayerNorm, timed alone over "
+                   f"{kp} calls enqueued ahead of the GPU; not part of the step"}
+    layer_flops = {k: qf + pf + uf + df + layers[k]["gflop"] * 1e9 for k in ("global", "local")}
+    encoder_layer = {
+        k: {"ms_per_layer": layer_ms[k], "tokens_per_s": whole_job_tokens_per_s(T, world, layer_ms[k]),
+            "tflops": layer_flops[k] / (layer_ms[k] / 1e3) / 1e12,
+            "calls": "ln_qkv, attention, out_proj, mlp (8 or 9 kernels)"}
+        for k in ("global", "local")}
+    encoder_layer["note"] = ("one whole encoder layer from the library's calls on the step's "
+                             f"packing, {kk} layers per event pair, enqueued ahead of the GPU; "
+                             "synthetic weights; not part of the step")
     g, lo = layers["global"], layers["local"]
     # The dominant kernel (the global layer's) against the tensor peak; the
     # local layer's kernel, HBM bound, against the copy bandwidth.  Kernel
@@ -506,6 +588,8 @@ def run_ours(args):
         "layers": layers,
         "out_proj": out_proj,
         "ln_qkv": ln_qkv,
+        "mlp": mlp,
+        "encoder_layer": encoder_layer,
         "roofline": roofline,
         "roofline_local": roofline_local,
         "gpu_launches": launches,

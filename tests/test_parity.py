@@ -230,3 +230,24 @@ def test_module_level_function(attn):
     torch.cuda.synchronize()
     ref, _ = oracle.attention_kind(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), "local")
     _compare(out.cpu(), ref, "module attention")
+
+
+@pytest.mark.parametrize("thetas", [(150000.0, 160000.0), (80000.0, 10000.0)])
+def test_sibling_checkpoint_bases(thetas):
+    """Checkpoints of the same shape whose RoPE bases differ ("ModernBertModel"
+    (safebydesign), "Implementing it": one lists 150000 global / 160000 local,
+    another 80000 / 10000) run through the same kernels with the bases in the
+    handle's configuration."""
+    tg, tl = thetas
+    h = binding.Attention(0, theta_global=tg, theta_local=tl)
+    try:
+        wl = W.config(2)
+        qkv, cu = wl.qkv.cuda(), wl.cu_seqlens.cuda()
+        for kind, theta in (("global", tg), ("local", tl)):
+            got = h.forward(qkv, cu, kind).cpu()
+            ref, _ = oracle.attention(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), theta,
+                                      oracle.KINDS[kind]["half_window"])
+            _compare(got, ref, f"{kind} theta {theta}")
+        assert h.get_error() == 0
+    finally:
+        h.close()
