@@ -291,6 +291,50 @@ def mlp(x_bits, norm_w_bits, wi_bits, wo_bits, eps: float = NORM_EPS, rows=None,
     return y
 
 
+def attention_padded(qkv_bits, mask, theta: float, half_window: int,
+                     heads: int = HEADS, head_dim: int = HEAD_DIM):
+    """The attention block over a padded batch, in its masked form, fp64.
+
+    qkv_bits: uint16 [B, S, 3 heads head_dim] bf16 bit patterns; mask: [B, S],
+    non-zero for a real token, 0 for a pad.  Inside attention the pads are
+    masked keys ("ModernBERT-base Architecture Teardown", the tokenizer with
+    padding=True: the 0s of the attention mask become a mask, so no real token
+    takes information from a pad; "Encoder-only models", "Padding and the key
+    padding mask": -inf at the ignored keys).  A real token's position is its
+    rank among the row's real tokens (its index in the row for right padding,
+    the tokenizer's form).  Query i admits key j iff both are real and, on a
+    local layer, |pos_i - pos_j| <= half_window.  A pad's row of the output is
+    0 (nothing downstream reads it).  Pure Python over rows and heads, for
+    small batches.  Returns fp64 [B, S, heads head_dim].
+    """
+    qkv = np.ascontiguousarray(qkv_bits)
+    m = np.asarray(mask) != 0
+    B, S, width = qkv.shape
+    assert m.shape == (B, S) and width == 3 * heads * head_dim
+    vals = (qkv.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    out = np.zeros((B, S, heads * head_dim), dtype=np.float64)
+    for b in range(B):
+        real = np.flatnonzero(m[b])
+        if real.size == 0:
+            continue
+        pos = np.cumsum(m[b]) - 1
+        adm = m[b][:, None] & m[b][None, :]
+        if half_window >= 0:
+            adm &= np.abs(pos[:, None] - pos[None, :]) <= half_window
+        for h in range(heads):
+            q = vals[b, :, h * head_dim:(h + 1) * head_dim]
+            k = vals[b, :, (heads + h) * head_dim:(heads + h + 1) * head_dim]
+            v = vals[b, :, (2 * heads + h) * head_dim:(2 * heads + h + 1) * head_dim]
+            Q = np.zeros((S, head_dim))
+            K = np.zeros((S, head_dim))
+            for t in real:
+                Q[t] = rope(q[t], int(pos[t]), theta)
+                K[t] = rope(k[t], int(pos[t]), theta)
+            _, o = sdpa_dense(Q, K, v, 1.0 / np.sqrt(head_dim), mask=adm)
+            out[b, :, h * head_dim:(h + 1) * head_dim] = o
+    return out
+
+
 def attention_kind(qkv_bits, cu_seqlens, kind: str, rows=None, threads: int = 0):
     """attention() with the constants of a ModernBERT-base layer kind."""
     p = KINDS[kind]
