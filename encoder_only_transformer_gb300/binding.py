@@ -38,6 +38,7 @@ SIGNATURES = {
     "mbert_attn_create": (_c_int, [ctypes.POINTER(_vp), ctypes.POINTER(Config), _c_int]),
     "mbert_attn_reserve": (_c_int, [_vp, _c_i64, _c_i64]),
     "mbert_attn_forward": (_c_int, [_vp, _vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp]),
+    "mbert_attn_forward_padded": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp]),
     "mbert_attn_key_counts": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp]),
     "mbert_attn_out_proj": (_c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _vp]),
     "mbert_attn_ln_qkv": (_c_int, [_vp, _vp, _vp, _vp, _c_i64, ctypes.c_float, _vp, _vp]),
@@ -202,6 +203,30 @@ class Attention:
         _check(st, "out_proj")
         return out
 
+    def forward_padded(self, qkv: torch.Tensor, attention_mask: torch.Tensor, layer_kind,
+                       out: torch.Tensor = None) -> torch.Tensor:
+        """out[B, S, 768] bf16 for a padded batch: qkv [B, S, 2304] bf16 and
+        attention_mask [B, S] int32 (1 = real token, 0 = pad) on this device;
+        pad rows of out are zeros."""
+        kind = _kind(layer_kind)
+        if qkv.dim() != 3 or qkv.shape[2] != QKV_WIDTH or qkv.dtype != torch.bfloat16 \
+                or qkv.device != self.device or not qkv.is_contiguous():
+            raise TypeError(f"qkv must be a contiguous bf16 [B, S, {QKV_WIDTH}] tensor on {self.device}")
+        B, S = qkv.shape[0], qkv.shape[1]
+        if (attention_mask.dtype != torch.int32 or tuple(attention_mask.shape) != (B, S)
+                or attention_mask.device != self.device or not attention_mask.is_contiguous()):
+            raise TypeError(f"attention_mask must be a contiguous int32 [{B}, {S}] tensor on {self.device}")
+        if out is None:
+            out = torch.empty(B, S, OUT_WIDTH, dtype=torch.bfloat16, device=self.device)
+        if (out.dtype != torch.bfloat16 or tuple(out.shape) != (B, S, OUT_WIDTH)
+                or out.device != self.device or not out.is_contiguous()):
+            raise TypeError(f"out must be a contiguous bf16 [{B}, {S}, {OUT_WIDTH}] tensor")
+        st = load_library().mbert_attn_forward_padded(self._h, qkv.data_ptr(),
+                                                      attention_mask.data_ptr(), B, S, kind,
+                                                      out.data_ptr(), _stream_ptr(self.device))
+        _check(st, "forward_padded")
+        return out
+
     def ln_qkv(self, x: torch.Tensor, norm_w, wqkv: torch.Tensor, eps: float = NORM_EPS,
                out: torch.Tensor = None) -> torch.Tensor:
         """qkv[T, 2304] bf16 = LayerNorm(x) Wqkv^T: the bias-free pre-attention
@@ -307,6 +332,15 @@ def attention(qkv: torch.Tensor, cu_seqlens: torch.Tensor, layer_kind, max_seqle
     if not qkv.is_cuda:
         raise ValueError("qkv must be a CUDA tensor")
     return _default(qkv.device).forward(qkv, cu_seqlens, layer_kind, max_seqlen, out)
+
+
+def attention_padded(qkv: torch.Tensor, attention_mask: torch.Tensor, layer_kind,
+                     out: torch.Tensor = None) -> torch.Tensor:
+    """The attention block for a padded batch: qkv [B, S, 2304] bf16 and
+    attention_mask [B, S] int32 (CUDA) -> out [B, S, 768], zeros at pads."""
+    if not qkv.is_cuda:
+        raise ValueError("qkv must be a CUDA tensor")
+    return _default(qkv.device).forward_padded(qkv, attention_mask, layer_kind, out)
 
 
 def ln_qkv(x: torch.Tensor, norm_w, wqkv: torch.Tensor, eps: float = NORM_EPS,

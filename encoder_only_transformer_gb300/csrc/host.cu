@@ -37,6 +37,12 @@ struct mbert_attn {
     int64_t ln_cap = 0;                     // rows
     __nv_bfloat16 *mid = nullptr;           // GELU(g) * u rows [mid_cap][1152] (mlp)
     int64_t mid_cap = 0;                    // rows
+    // the padded-batch call: packed qkv and out, each padded token's rank
+    // among its row's real tokens, the row lengths and their cu_seqlens
+    __nv_bfloat16 *pad_qkv = nullptr, *pad_out = nullptr;
+    int64_t pad_qkv_cap = 0, pad_out_cap = 0;
+    int32_t *pad_idx = nullptr, *pad_len = nullptr, *pad_cu = nullptr;
+    int64_t pad_idx_cap = 0, pad_seq_cap = 0;
     // global layers: split of the (entry, head, key tile) iterations among
     // one persistent CTA per SM
     int32_t *tile_start = nullptr;          // [entries + 1]
@@ -148,8 +154,6 @@ int grow_workspace(mbert_attn *h, int64_t entries, int64_t rot_rows)
         if (h->rot) {
             cudaDeviceSynchronize();
             cudaFree(h->rot);
-        cudaFree(h->ln);
-        cudaFree(h->mid);
         }
         h->rot = r;
         h->rot_cap = cap;
@@ -314,6 +318,13 @@ MBERT_API void mbert_attn_destroy(mbert_attn *h)
         cudaFree(h->tile_start);
         cudaFree(h->unit_cnt);
         cudaFree(h->partials);
+        cudaFree(h->ln);
+        cudaFree(h->mid);
+        cudaFree(h->pad_qkv);
+        cudaFree(h->pad_out);
+        cudaFree(h->pad_idx);
+        cudaFree(h->pad_len);
+        cudaFree(h->pad_cu);
     }
     delete h;
 }
@@ -435,9 +446,14 @@ MBERT_API int mbert_attn_reserve(mbert_attn *h, int64_t max_tokens, int64_t max_
     return grow_workspace(h, entry_bound(max_tokens, max_seqs), max_tokens);
 }
 
-MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *cu_seqlens,
-                                 int n_seqs, int64_t total_tokens, int max_seqlen,
-                                 int layer_kind, void *out, void *stream)
+namespace {
+
+// The attention call.  cu_short: the packed rows past cu[n_seqs] belong to
+// no sequence (cu[n_seqs] <= total_tokens, checked on the device); the plan
+// kernel then schedules local layers too.
+int forward_impl(mbert_attn *h, const void *qkv, const int32_t *cu_seqlens, int n_seqs,
+                 int64_t total_tokens, int max_seqlen, int layer_kind, void *out, void *stream,
+                 bool cu_short)
 {
     int rc = check_common(h, cu_seqlens, n_seqs, total_tokens, max_seqlen, layer_kind);
     if (rc != MBERT_OK)
@@ -459,6 +475,7 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
     if (rc != MBERT_OK)
         return rc;
     Plan p = make_plan(h, cu_seqlens, n_seqs, T, max_seqlen);
+    p.cu_short_ok = cu_short;
     if (layer_kind == MBERT_GLOBAL) {
         // the global kernel takes 256 query rows (two 128-row tiles) per
         // entry and splits all iterations evenly among one CTA per SM
@@ -507,7 +524,7 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
         la.work_count = nullptr;
         la.block_bound = p.entry_bound;
         la.num_ctas = h->num_sms;
-        if (n_seqs > kLocalSelfScheduleMaxSeqs) {
+        if (n_seqs > kLocalSelfScheduleMaxSeqs || cu_short) {
             e = launch_plan(p, st);
             la.work = h->work;
             la.work_count = h->work_count;
@@ -534,6 +551,90 @@ MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *
     if (e == cudaSuccess && ev1)
         e = cudaEventRecord(ev1, st);
     h->launches += 3;
+    h->last_stream = st;
+    return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+MBERT_API int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *cu_seqlens,
+                                 int n_seqs, int64_t total_tokens, int max_seqlen,
+                                 int layer_kind, void *out, void *stream)
+{
+    return forward_impl(h, qkv, cu_seqlens, n_seqs, total_tokens, max_seqlen, layer_kind, out,
+                        stream, false);
+}
+
+MBERT_API int mbert_attn_forward_padded(mbert_attn *h, const void *qkv, const int32_t *attention_mask,
+                                        int batch, int seq_len, int layer_kind, void *out,
+                                        void *stream)
+{
+    if (!h || batch < 0 || seq_len < 0 || (layer_kind != MBERT_GLOBAL && layer_kind != MBERT_LOCAL))
+        return MBERT_ERR_BAD_ARG;
+    if (seq_len > h->cfg.max_seqlen)
+        return MBERT_ERR_SEQ_TOO_LONG;
+    const int64_t rows = static_cast<int64_t>(batch) * seq_len;
+    if (rows > INT32_MAX)
+        return MBERT_ERR_BAD_ARG;
+    if (rows == 0)
+        return MBERT_OK;
+    if (!qkv || !attention_mask || !out)
+        return MBERT_ERR_BAD_ARG;
+    if ((reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
+        (reinterpret_cast<uintptr_t>(attention_mask) & 3))
+        return MBERT_ERR_BAD_ARG;
+    if (ranges_overlap(qkv, static_cast<size_t>(rows) * kQKVWidth * 2, out,
+                       static_cast<size_t>(rows) * kHidden * 2) ||
+        ranges_overlap(attention_mask, static_cast<size_t>(rows) * 4, out,
+                       static_cast<size_t>(rows) * kHidden * 2))
+        return MBERT_ERR_BAD_ARG;
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = grow_rows(&h->pad_qkv, &h->pad_qkv_cap, rows, kQKVWidth);
+    if (rc == MBERT_OK)
+        rc = grow_rows(&h->pad_out, &h->pad_out_cap, rows, kHidden);
+    if (rc == MBERT_OK && (rows > h->pad_idx_cap || batch + 1 > h->pad_seq_cap)) {
+        const int64_t ri = rows > h->pad_idx_cap ? (rows < 8192 ? 8192 : rows) : h->pad_idx_cap;
+        const int64_t si = batch + 1 > h->pad_seq_cap ? (batch + 1 < 1024 ? 1024 : batch + 1)
+                                                       : h->pad_seq_cap;
+        int32_t *idx = nullptr, *len = nullptr, *cu = nullptr;
+        if (cudaMalloc(&idx, sizeof(int32_t) * ri) != cudaSuccess ||
+            cudaMalloc(&len, sizeof(int32_t) * si) != cudaSuccess ||
+            cudaMalloc(&cu, sizeof(int32_t) * si) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(idx);
+            cudaFree(len);
+            return MBERT_ERR_OOM;
+        }
+        if (h->pad_idx) {
+            cudaDeviceSynchronize();
+            cudaFree(h->pad_idx);
+            cudaFree(h->pad_len);
+            cudaFree(h->pad_cu);
+        }
+        h->pad_idx = idx;
+        h->pad_len = len;
+        h->pad_cu = cu;
+        h->pad_idx_cap = ri;
+        h->pad_seq_cap = si;
+    }
+    if (rc != MBERT_OK)
+        return rc;
+    cudaError_t e = launch_mask_scan(attention_mask, batch, seq_len, h->pad_idx, h->pad_len,
+                                     h->pad_cu, st);
+    if (e == cudaSuccess)
+        e = launch_gather_rows(static_cast<const __nv_bfloat16 *>(qkv), h->pad_idx, h->pad_cu,
+                               batch, seq_len, kQKVWidth, h->pad_qkv, h->num_sms, st);
+    h->launches += 3;
+    if (e != cudaSuccess)
+        return fail_cuda(e);
+    rc = forward_impl(h, h->pad_qkv, h->pad_cu, batch, rows, seq_len, layer_kind, h->pad_out,
+                      stream, true);
+    if (rc != MBERT_OK)
+        return rc;
+    e = launch_scatter_rows(h->pad_out, h->pad_idx, h->pad_cu, batch, seq_len, kHidden,
+                            static_cast<__nv_bfloat16 *>(out), h->num_sms, st);
+    h->launches += 1;
     h->last_stream = st;
     return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
 }

@@ -23,6 +23,7 @@ struct Plan {
     int32_t *work_count;    // device scalar: entries written (0 if the checks failed)
     int entry_bound;        // host-side upper bound on the entry count
     int32_t *err;           // device error word (sticky, bit mask)
+    bool cu_short_ok = false;   // accept cu[n] <= T: rows past cu[n] belong to no sequence
     // Optional (global layers): tile_start[e] = sum over entries before e of
     // heads * ceil(L/128) (the entry's first iteration in the split of all
     // (entry, head, key tile) iterations among persistent CTAs), with
@@ -137,6 +138,21 @@ cudaError_t launch_mlp_down(const OutProjArgs &a, cudaStream_t stream);
 // into h [T][768] (bf16): one warp per row, fp32 statistics.
 cudaError_t launch_layernorm(const __nv_bfloat16 *x, const __nv_bfloat16 *w, long long T,
                              float eps, __nv_bfloat16 *h, int num_sms, cudaStream_t stream);
+
+// The padded-batch form [B][S] with a 0/1 attention mask, to and from the
+// packed form: mask_scan writes, per row b, each real token's rank among the
+// row's real tokens (-1 for a pad) and the row's count, then the exclusive
+// prefix sum of the counts as cu_seqlens[0..B]; gather copies every real
+// token's qkv row to packed row cu[b] + rank; scatter writes every padded
+// row of out from its packed row, zeros for pads.
+cudaError_t launch_mask_scan(const int32_t *mask, int B, int S, int32_t *rank, int32_t *len,
+                             int32_t *cu, cudaStream_t stream);
+cudaError_t launch_gather_rows(const __nv_bfloat16 *src, const int32_t *rank, const int32_t *cu,
+                               int B, int S, int width, __nv_bfloat16 *dst, int num_sms,
+                               cudaStream_t stream);
+cudaError_t launch_scatter_rows(const __nv_bfloat16 *src, const int32_t *rank, const int32_t *cu,
+                                int B, int S, int width, __nv_bfloat16 *dst, int num_sms,
+                                cudaStream_t stream);
 
 // Number of sequences up to which the local kernel finds its blocks itself
 // (above it the plan kernel writes a work list first).

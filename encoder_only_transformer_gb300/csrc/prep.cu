@@ -39,14 +39,15 @@ __device__ int block_inclusive_scan(int v, int *warp_sums)
     return v;
 }
 
-// One block.  Checks cu_seqlens (cu[0] == 0, non-decreasing, cu[n] == T,
-// every length <= max_seqlen) and writes the work list: for each sequence,
+// One block.  Checks cu_seqlens (cu[0] == 0, non-decreasing, cu[n] == T --
+// or cu[n] <= T with cu_short_ok, when rows past the last sequence belong to
+// none -- every length <= max_seqlen) and writes the work list: for each sequence,
 // its ceil(L/blk) query blocks of blk rows, sequences ordered by decreasing block count
 // (longest-processing-time first; the order inside a bin is arbitrary and
 // does not affect any result).
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seqlen, int blk,
-            int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count,
+            int cu_short_ok, int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count,
             int32_t *__restrict__ tile_start, int32_t *__restrict__ unit_cnt)
 {
     __shared__ int s_bad;
@@ -61,7 +62,8 @@ plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seq
     for (int i = tid; i <= kMaxBins; i += kPlanThreads)
         s_hist[i] = 0;
     __syncthreads();
-    if (tid == 0 && (cu[0] != 0 || static_cast<long long>(cu[n_seqs]) != T))
+    if (tid == 0 && (cu[0] != 0 || (cu_short_ok ? static_cast<long long>(cu[n_seqs]) > T
+                                                : static_cast<long long>(cu[n_seqs]) != T)))
         atomicOr(&s_bad, kErrBadCu);
     for (int s = tid; s < n_seqs; s += kPlanThreads) {
         const int L = cu[s + 1] - cu[s];
@@ -275,7 +277,7 @@ cudaError_t launch_wait_timeout_selftest(int32_t *err, unsigned long long limit_
 cudaError_t launch_plan(const Plan &p, cudaStream_t stream)
 {
     plan_kernel<<<1, kPlanThreads, 0, stream>>>(p.cu, p.n_seqs, p.T, p.max_seqlen, p.block,
-                                                  p.err, p.work, p.work_count, p.tile_start,
+                                                  p.cu_short_ok ? 1 : 0, p.err, p.work, p.work_count, p.tile_start,
                                                   p.unit_cnt);
     return cudaGetLastError();
 }

@@ -110,6 +110,28 @@ int mbert_attn_forward(mbert_attn *h, const void *qkv, const int32_t *cu_seqlens
                        int n_seqs, int64_t total_tokens, int max_seqlen,
                        int layer_kind, void *out, void *stream);
 
+/* The attention block for a padded batch: B rows of S tokens with an
+ * attention mask of 1 for a real token and 0 for a pad ("ModernBERT-base
+ * Architecture Teardown", the tokenizer with padding=True: the 0s of the
+ * mask become a mask inside attention, so no real token takes information
+ * from a pad; "Encoder-only models", "Padding and the key padding mask").
+ * Each row's real tokens, in order, are one sequence: a real token's
+ * position is its rank among its row's real tokens (its index for a
+ * right-padded row), and only real tokens of the same row are keys.
+ *   qkv             device bf16 [batch][seq_len][2304], 16-byte aligned.
+ *   attention_mask  device int32 [batch][seq_len]: non-zero = real token.
+ *   seq_len         <= the handle's max_seqlen (else MBERT_ERR_SEQ_TOO_LONG);
+ *                   batch * seq_len < 2^31.
+ *   out             device bf16 [batch][seq_len][768], 16-byte aligned, must
+ *                   not overlap qkv or the mask.  Every row is written: a
+ *                   real token's attention output, zeros for a pad.
+ * The call packs the real rows into handle-owned buffers (grown with
+ * cudaMalloc when needed), runs mbert_attn_forward's kernels on them and
+ * unpacks the result, all on `stream`; calls sharing a handle must not
+ * overlap on the GPU.  Returns as mbert_attn_forward. */
+int mbert_attn_forward_padded(mbert_attn *h, const void *qkv, const int32_t *attention_mask,
+                              int batch, int seq_len, int layer_kind, void *out, void *stream);
+
 /* Debug/verification entry: for every packed row, the number of keys the
  * attention kernel's tile schedule and mask admit for that query (the size
  * of its admitted set), computed by the same device code the forward pass
