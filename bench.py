@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from encoder_only_transformer_gb300 import workloads as W  # noqa: E402
@@ -415,6 +416,44 @@ def run_ours(args):
         layer_ms[kind] = max_over_ranks(a.elapsed_time(b), world, dev) / kk
     del lay_qkv, lay_a, lay_x1
 
+    # --- the padded-batch call: 8 rows of 2048 positions holding sequences
+    # of U{128..2048} real tokens (seeded), each layer kind, against the
+    # packed call on the same tokens
+    rng = np.random.default_rng(4245)
+    pad_B, pad_S = 8, 2048
+    pad_len = rng.integers(128, pad_S + 1, pad_B)
+    pad_mask = torch.zeros(pad_B, pad_S, dtype=torch.int32)
+    for bb, Lb in enumerate(pad_len):
+        pad_mask[bb, :Lb] = 1
+    gp = torch.Generator().manual_seed(4245)
+    pad_qkv = torch.randn(pad_B, pad_S, 2304, generator=gp).to(torch.bfloat16).to(dev)
+    pad_mask = pad_mask.to(dev)
+    pad_out = torch.empty(pad_B, pad_S, 768, dtype=torch.bfloat16, device=dev)
+    pk_qkv = torch.cat([pad_qkv[bb, :Lb] for bb, Lb in enumerate(pad_len)])
+    pk_cu = torch.tensor(np.concatenate([[0], np.cumsum(pad_len)]), dtype=torch.int32, device=dev)
+    pk_out = torch.empty(pk_qkv.shape[0], 768, dtype=torch.bfloat16, device=dev)
+    padded = {"batch": pad_B, "seq_len": pad_S, "real_tokens": int(pad_len.sum())}
+    for kind in ("global", "local"):
+        res = {}
+        for name, call in (("padded", lambda: attn.forward_padded(pad_qkv, pad_mask, kind, out=pad_out)),
+                           ("packed", lambda: attn.forward(pk_qkv, pk_cu, kind, max_seqlen=pad_S, out=pk_out))):
+            for _ in range(3):
+                call()
+            barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            queue_ahead(kk)
+            a.record()
+            for _ in range(kk):
+                call()
+            b.record()
+            barrier()
+            res[name] = max_over_ranks(a.elapsed_time(b), world, dev) / kk
+        padded[kind] = {"ms_padded": res["padded"], "ms_packed": res["packed"],
+                        "real_tokens_per_s": int(pad_len.sum()) / (res["padded"] / 1e3)}
+    padded["note"] = ("forward_padded (pack, attention kernels, unpack) against forward on the "
+                      "same tokens packed; not part of the step")
+    del pad_qkv, pad_out, pk_qkv, pk_out
+
     # --- end to end through the public API, pinned host buffers.  Every step
     # uploads both layers' qkv and reads both outputs back.  Copies and
     # compute are pipelined the way a serving loop would run them: uploads
@@ -590,6 +629,7 @@ def run_ours(args):
         "ln_qkv": ln_qkv,
         "mlp": mlp,
         "encoder_layer": encoder_layer,
+        "padded": padded,
         "roofline": roofline,
         "roofline_local": roofline_local,
         "gpu_launches": launches,

@@ -124,12 +124,14 @@ move_rows_kernel(const __nv_bfloat16 *__restrict__ src, const int32_t *__restric
     }
     if (!kScatter) {
         // packed rows past the last sequence hold no token; the attention
-        // kernels load them inside a sequence's last tile (as keys they are
-        // masked, as values they meet a zero weight), so they must be finite:
-        // zero them
+        // kernels load the first of them inside the last sequence's last
+        // tiles (as keys they are masked, as values they meet a zero weight,
+        // so they must be finite): zero the 256 rows that a tile of 256
+        // query rows or a key tile with the band's reach can touch
         const long long used = cu[B];
+        const long long end = used + 256 < rows ? used + 256 : rows;
         for (long long r = used + static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-             r < rows; r += stride) {
+             r < end; r += stride) {
             uint4 *d = reinterpret_cast<uint4 *>(dst + r * width);
             for (int v = lane; v < vecs; v += 32)
                 d[v] = make_uint4(0u, 0u, 0u, 0u);
