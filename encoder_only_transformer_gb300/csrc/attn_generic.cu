@@ -43,6 +43,7 @@ attn_generic_kernel(const __grid_constant__ CUtensorMap tm_rot,
                     const int32_t *__restrict__ work_count, int hw,
                     __nv_bfloat16 *__restrict__ out, int32_t *err)
 {
+    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -245,6 +246,7 @@ attn_generic_kernel(const __grid_constant__ CUtensorMap tm_rot,
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -261,9 +263,8 @@ cudaError_t launch_attn_generic(const AttnArgs &a, cudaStream_t stream)
         configured = true;
     }
     const long long grid = static_cast<long long>(a.entry_bound) * kHeads;
-    attn_generic_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
+    return launch_chained(attn_generic_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, stream,
         a.tm_rot, a.tm_qkv, a.cu, a.work, a.work_count, a.half_window, a.out, a.err);
-    return cudaGetLastError();
 }
 
 }  // namespace mbert

@@ -511,6 +511,7 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
                    int32_t *__restrict__ unit_cnt, float *__restrict__ partials,
                    __nv_bfloat16 *__restrict__ out, int32_t *err)
 {
+    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     Ctx c;
@@ -593,6 +594,7 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
         tc_fence_after();
         tmem_dealloc(c.tmem, kTmemCols);
     }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -610,10 +612,9 @@ cudaError_t launch_attn_global(const AttnArgs &a, cudaStream_t stream)
             return e;
         configured[dev] = true;
     }
-    attn_global_kernel<<<a.num_ctas, kThreads, kSmemBytes, stream>>>(
+    return launch_chained(attn_global_kernel, dim3(a.num_ctas), dim3(kThreads), kSmemBytes, stream,
         a.tm_rot, a.tm_qkv, a.cu, a.work, a.work_count, a.tile_start, a.unit_cnt, a.partials,
         a.out, a.err);
-    return cudaGetLastError();
 }
 
 }  // namespace mbert

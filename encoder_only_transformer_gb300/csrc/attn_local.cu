@@ -288,6 +288,7 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
                   const int2 *__restrict__ work, const int32_t *__restrict__ work_count, int hw,
                   __nv_bfloat16 *__restrict__ out, int32_t *err)
 {
+    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     __shared__ long long s_range[2];
     __shared__ int s_g;
@@ -905,6 +906,7 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -926,10 +928,9 @@ cudaError_t launch_attn_local(const LocalArgs &a, cudaStream_t stream)
     const long long grid = units < a.num_ctas ? units : a.num_ctas;
     if (grid <= 0)
         return cudaSuccess;
-    attn_local_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
+    return launch_chained(attn_local_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, stream,
         a.tm_qkv, a.tm_out, a.rope, a.cu, a.n_seqs, a.T, a.max_seqlen, a.work, a.work_count,
         a.half_window, a.out, a.err);
-    return cudaGetLastError();
 }
 
 }  // namespace mbert

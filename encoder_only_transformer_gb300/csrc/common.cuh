@@ -130,6 +130,16 @@ __device__ __forceinline__ uint32_t elect_one_sync()
     return pred;
 }
 
+// ---- programmatic dependent launch ----
+// Every kernel is launched so that its launch may overlap the end of the
+// kernel before it in the stream.  A kernel calls pdl_wait() before its
+// first global-memory access (it returns once the previous kernel has
+// completed and its writes are visible; at once if there is none), and
+// pdl_trigger() when its own work is done, which lets the next kernel's
+// launch begin before this grid has fully retired.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- thread-block clusters ----
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {

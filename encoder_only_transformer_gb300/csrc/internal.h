@@ -9,6 +9,26 @@
 
 namespace mbert {
 
+// Launch `kernel` on `stream` with programmatic stream serialization: its
+// launch may overlap the tail of the previous kernel in the stream, which
+// it waits for in-kernel (pdl_wait) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kPairsConst = 32;
 
 // Work list written by the plan kernel: one entry per (sequence, 128-query

@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 layernorm_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ w,
                  long long T, float eps, __nv_bfloat16 *__restrict__ h)
 {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long first = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     const long long stride = static_cast<long long>(gridDim.x) * kWarpsPerBlock;
@@ -82,6 +83,7 @@ layernorm_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__res
             hr[lane + 32 * j] = o;
         }
     }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -94,8 +96,8 @@ cudaError_t launch_layernorm(const __nv_bfloat16 *x, const __nv_bfloat16 *w, lon
     const long long need = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const long long cap = static_cast<long long>(num_sms) * 8;      // 64 resident warps per SM
     const int grid = static_cast<int>(need < cap ? need : cap);
-    layernorm_kernel<<<grid, 32 * kWarpsPerBlock, 0, stream>>>(x, w, T, eps, h);
-    return cudaGetLastError();
+    return launch_chained(layernorm_kernel, dim3(grid), dim3(32 * kWarpsPerBlock), 0, stream, x, w, T,
+                          eps, h);
 }
 
 }  // namespace mbert

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(kScanThreads)
 mask_rows_kernel(const int32_t *__restrict__ mask, int S, int32_t *__restrict__ rank,
                  int32_t *__restrict__ len)
 {
+    pdl_wait();
     const int b = blockIdx.x;
     const int32_t *m = mask + static_cast<size_t>(b) * S;
     int32_t *rk = rank + static_cast<size_t>(b) * S;
@@ -73,11 +74,13 @@ mask_rows_kernel(const int32_t *__restrict__ mask, int S, int32_t *__restrict__ 
     }
     if (threadIdx.x == 0)
         len[b] = carry;
+    pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kScanThreads)
 mask_offsets_kernel(const int32_t *__restrict__ len, int B, int32_t *__restrict__ cu)
 {
+    pdl_wait();
     int carry = 0;
     for (int b0 = 0; b0 < B; b0 += kScanThreads) {
         const int b = b0 + threadIdx.x;
@@ -90,6 +93,7 @@ mask_offsets_kernel(const int32_t *__restrict__ len, int B, int32_t *__restrict_
     }
     if (threadIdx.x == 0)
         cu[B] = carry;
+    pdl_trigger();
 }
 
 // One warp per padded row: a real row moves between padded row b S + s and
@@ -100,6 +104,7 @@ move_rows_kernel(const __nv_bfloat16 *__restrict__ src, const int32_t *__restric
                  const int32_t *__restrict__ cu, int B, int S, int width,
                  __nv_bfloat16 *__restrict__ dst)
 {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long rows = static_cast<long long>(B) * S;
     const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
@@ -137,6 +142,7 @@ move_rows_kernel(const __nv_bfloat16 *__restrict__ src, const int32_t *__restric
                 d[v] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
+    pdl_trigger();
 }
 
 int move_grid(int B, int S, int num_sms)
@@ -154,9 +160,11 @@ cudaError_t launch_mask_scan(const int32_t *mask, int B, int S, int32_t *rank, i
 {
     if (B <= 0)
         return cudaSuccess;
-    mask_rows_kernel<<<B, kScanThreads, 0, stream>>>(mask, S, rank, len);
-    mask_offsets_kernel<<<1, kScanThreads, 0, stream>>>(len, B, cu);
-    return cudaGetLastError();
+    cudaError_t e = launch_chained(mask_rows_kernel, dim3(B), dim3(kScanThreads), 0, stream, mask,
+                                   S, rank, len);
+    if (e == cudaSuccess)
+        e = launch_chained(mask_offsets_kernel, dim3(1), dim3(kScanThreads), 0, stream, len, B, cu);
+    return e;
 }
 
 cudaError_t launch_gather_rows(const __nv_bfloat16 *src, const int32_t *rank, const int32_t *cu,
@@ -165,9 +173,8 @@ cudaError_t launch_gather_rows(const __nv_bfloat16 *src, const int32_t *rank, co
 {
     if (B <= 0 || S <= 0)
         return cudaSuccess;
-    move_rows_kernel<false><<<move_grid(B, S, num_sms), 256, 0, stream>>>(src, rank, cu, B, S,
-                                                                             width, dst);
-    return cudaGetLastError();
+    return launch_chained(move_rows_kernel<false>, dim3(move_grid(B, S, num_sms)), dim3(256), 0,
+                          stream, src, rank, cu, B, S, width, dst);
 }
 
 cudaError_t launch_scatter_rows(const __nv_bfloat16 *src, const int32_t *rank, const int32_t *cu,
@@ -176,9 +183,8 @@ cudaError_t launch_scatter_rows(const __nv_bfloat16 *src, const int32_t *rank, c
 {
     if (B <= 0 || S <= 0)
         return cudaSuccess;
-    move_rows_kernel<true><<<move_grid(B, S, num_sms), 256, 0, stream>>>(src, rank, cu, B, S,
-                                                                            width, dst);
-    return cudaGetLastError();
+    return launch_chained(move_rows_kernel<true>, dim3(move_grid(B, S, num_sms)), dim3(256), 0,
+                          stream, src, rank, cu, B, S, width, dst);
 }
 
 }  // namespace mbert

@@ -50,6 +50,7 @@ plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seq
             int cu_short_ok, int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count,
             int32_t *__restrict__ tile_start, int32_t *__restrict__ unit_cnt)
 {
+    pdl_wait();
     __shared__ int s_bad;
     __shared__ int s_hist[kMaxBins + 1];
     __shared__ int s_off[kMaxBins + 1];
@@ -137,6 +138,7 @@ plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seq
         tile_start[total] = s_carry;
     for (int i = tid; i < total * kHeads; i += kPlanThreads)
         unit_cnt[i] = 0;
+    pdl_trigger();
 }
 
 // Sequence index of packed row `row` (cu validated, non-decreasing).
@@ -166,6 +168,7 @@ rope_qk_kernel(const __nv_bfloat16 *__restrict__ qkv, const int32_t *__restrict_
                long long T, const float2 *__restrict__ table, int table_rows,
                const int32_t *__restrict__ work_count, __nv_bfloat16 *__restrict__ rot)
 {
+    pdl_wait();
     if (*work_count <= 0)
         return;   // the plan's checks failed: positions are unknown
     const long long row = static_cast<long long>(blockIdx.x) * kRopeRowsPerCta
@@ -201,6 +204,7 @@ rope_qk_kernel(const __nv_bfloat16 *__restrict__ qkv, const int32_t *__restrict_
     constexpr int kRotWidth = 2 * kHidden;
     *reinterpret_cast<uint4 *>(rot + row * kRotWidth + col) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
     *reinterpret_cast<uint4 *>(rot + row * kRotWidth + col + kPairs) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+    pdl_trigger();
 }
 
 // One CTA of 128 threads per work entry; thread r is query position
@@ -211,6 +215,7 @@ __global__ void __launch_bounds__(kBlockM)
 key_count_kernel(const int32_t *__restrict__ cu, const int2 *__restrict__ work,
                  const int32_t *__restrict__ work_count, int hw, int32_t *__restrict__ counts)
 {
+    pdl_wait();
     if (static_cast<int>(blockIdx.x) >= *work_count)
         return;
     const int2 e = work[blockIdx.x];
@@ -249,6 +254,7 @@ key_count_kernel(const int32_t *__restrict__ cu, const int2 *__restrict__ work,
     }
     if (qpos < L)
         counts[row0 + qpos] = cnt;
+    pdl_trigger();
 }
 
 // Self-test of the bounded wait: one thread initialises an mbarrier that
@@ -276,26 +282,24 @@ cudaError_t launch_wait_timeout_selftest(int32_t *err, unsigned long long limit_
 
 cudaError_t launch_plan(const Plan &p, cudaStream_t stream)
 {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(p.cu, p.n_seqs, p.T, p.max_seqlen, p.block,
-                                                  p.cu_short_ok ? 1 : 0, p.err, p.work, p.work_count, p.tile_start,
-                                                  p.unit_cnt);
-    return cudaGetLastError();
+    return launch_chained(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, p.cu, p.n_seqs, p.T,
+                          p.max_seqlen, p.block, p.cu_short_ok ? 1 : 0, p.err, p.work,
+                          p.work_count, p.tile_start, p.unit_cnt);
 }
 
 cudaError_t launch_rope_qk(const Plan &p, const __nv_bfloat16 *qkv, const float2 *table,
                            int table_rows, __nv_bfloat16 *rot, cudaStream_t stream)
 {
     const long long blocks = (p.T + kRopeRowsPerCta - 1) / kRopeRowsPerCta;
-    rope_qk_kernel<<<static_cast<unsigned>(blocks), kRopeRowsPerCta * kRopeThreadsPerRow, 0,
-                     stream>>>(qkv, p.cu, p.n_seqs, p.T, table, table_rows, p.work_count, rot);
-    return cudaGetLastError();
+    return launch_chained(rope_qk_kernel, dim3(static_cast<unsigned>(blocks)),
+                          dim3(kRopeRowsPerCta * kRopeThreadsPerRow), 0, stream, qkv, p.cu, p.n_seqs,
+                          p.T, table, table_rows, p.work_count, rot);
 }
 
 cudaError_t launch_key_count(const Plan &p, int half_window, int32_t *counts, cudaStream_t stream)
 {
-    key_count_kernel<<<p.entry_bound, kBlockM, 0, stream>>>(p.cu, p.work, p.work_count,
-                                                            half_window, counts);
-    return cudaGetLastError();
+    return launch_chained(key_count_kernel, dim3(p.entry_bound), dim3(kBlockM), 0, stream, p.cu,
+                          p.work, p.work_count, half_window, counts);
 }
 
 }  // namespace mbert

@@ -492,14 +492,18 @@ out_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                 const __nv_bfloat16 *x, long long T, int n_units, int32_t *err)
 {
+    pdl_wait();
     pair_gemm<kHidden / kBK, kHidden / kBN, Epi::kResidual>(tm_a, tm_w, tm_x, tm_y, x, T, n_units, err);
+    pdl_trigger();
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_y, long long T, int n_units, int32_t *err)
 {
+    pdl_wait();
     pair_gemm<kHidden / kBK, kQKVWidth / kBN, Epi::kPlain>(tm_a, tm_w, tm_y, tm_y, nullptr, T, n_units, err);
+    pdl_trigger();
 }
 
 // The MLP's first GEMM with its GeGLU: m = GELU(h Wi_g^T) * (h Wi_u^T),
@@ -508,7 +512,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mlp_up_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_y, long long T, int n_units, int32_t *err)
 {
+    pdl_wait();
     pair_gemm<kHidden / kBK, kInner / (kBN / 2), Epi::kGeglu>(tm_a, tm_w, tm_y, tm_y, nullptr, T, n_units, err);
+    pdl_trigger();
 }
 
 // The MLP's second GEMM with the residual: y = x + m Wo^T, K = 1152.
@@ -517,7 +523,9 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                 const __nv_bfloat16 *x, long long T, int n_units, int32_t *err)
 {
+    pdl_wait();
     pair_gemm<kInner / kBK, kHidden / kBN, Epi::kResidual>(tm_a, tm_w, tm_x, tm_y, x, T, n_units, err);
+    pdl_trigger();
 }
 
 // Pairs of CTAs to launch for `kernel`: as many as fit at once (per device,
@@ -560,9 +568,8 @@ cudaError_t launch_out_proj(const OutProjArgs &a, cudaStream_t stream)
     cudaError_t e = pair_count(out_proj_kernel, max_pairs, a.num_ctas, n_units, &pairs);
     if (e != cudaSuccess)
         return e;
-    out_proj_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(
+    return launch_chained(out_proj_kernel, dim3(2 * pairs), dim3(kThreads), kSmemBytes, stream,
         a.tm_a, a.tm_w, a.tm_x, a.tm_y, a.x, a.T, static_cast<int>(n_units), a.err);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_mlp_down(const OutProjArgs &a, cudaStream_t stream)
@@ -575,9 +582,8 @@ cudaError_t launch_mlp_down(const OutProjArgs &a, cudaStream_t stream)
     cudaError_t e = pair_count(mlp_down_kernel, max_pairs, a.num_ctas, n_units, &pairs);
     if (e != cudaSuccess)
         return e;
-    mlp_down_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(
+    return launch_chained(mlp_down_kernel, dim3(2 * pairs), dim3(kThreads), kSmemBytes, stream,
         a.tm_a, a.tm_w, a.tm_x, a.tm_y, a.x, a.T, static_cast<int>(n_units), a.err);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_qkv_proj(const QkvProjArgs &a, cudaStream_t stream)
@@ -590,9 +596,8 @@ cudaError_t launch_qkv_proj(const QkvProjArgs &a, cudaStream_t stream)
     cudaError_t e = pair_count(qkv_proj_kernel, max_pairs, a.num_ctas, n_units, &pairs);
     if (e != cudaSuccess)
         return e;
-    qkv_proj_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(
+    return launch_chained(qkv_proj_kernel, dim3(2 * pairs), dim3(kThreads), kSmemBytes, stream,
         a.tm_a, a.tm_w, a.tm_y, a.T, static_cast<int>(n_units), a.err);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_mlp_up(const QkvProjArgs &a, cudaStream_t stream)
@@ -605,9 +610,8 @@ cudaError_t launch_mlp_up(const QkvProjArgs &a, cudaStream_t stream)
     cudaError_t e = pair_count(mlp_up_kernel, max_pairs, a.num_ctas, n_units, &pairs);
     if (e != cudaSuccess)
         return e;
-    mlp_up_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(
+    return launch_chained(mlp_up_kernel, dim3(2 * pairs), dim3(kThreads), kSmemBytes, stream,
         a.tm_a, a.tm_w, a.tm_y, a.T, static_cast<int>(n_units), a.err);
-    return cudaGetLastError();
 }
 
 }  // namespace mbert
