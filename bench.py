@@ -49,16 +49,20 @@ N_SETS = 6
 # profiles/*_kernel_config3.md.  Reported only while the
 # kernel sources still hash to what was captured.
 NCU_TRAFFIC = {
-    "global": {"bytes": 39.64e6, "kernel": "attn_global_kernel",
-               "sources": {"attn_global.cu": "89c3d2ad0d680903", "common.cuh": "c49de87f54892de8"}},
+    "global": {"bytes": 39.58e6, "kernel": "attn_global_kernel",
+               "sources": {"attn_global.cu": "e38807e445b93991", "common.cuh": "c9dc0987f95761ca"}},
     "local": {"bytes": 37.83e6, "kernel": "attn_local_kernel",
-              "sources": {"attn_local.cu": "10494098048f75a4", "common.cuh": "c49de87f54892de8"}},
+              "sources": {"attn_local.cu": "deffadc935560231", "common.cuh": "c9dc0987f95761ca"}},
     "out_proj": {"bytes": 26.38e6, "kernel": "out_proj_kernel",
-                 "sources": {"projections.cu": "8da80e046fce28c7", "common.cuh": "c49de87f54892de8"}},
+                 "sources": {"projections.cu": "e291db50f03adf3f", "common.cuh": "c9dc0987f95761ca"}},
     "qkv_proj": {"bytes": 16.20e6, "kernel": "qkv_proj_kernel",
-                 "sources": {"projections.cu": "8da80e046fce28c7", "common.cuh": "c49de87f54892de8"}},
+                 "sources": {"projections.cu": "e291db50f03adf3f", "common.cuh": "c9dc0987f95761ca"}},
     "layernorm": {"bytes": 12.59e6, "kernel": "layernorm_kernel",
-                  "sources": {"layernorm.cu": "bb3e0cd506f60c79", "common.cuh": "c49de87f54892de8"}},
+                  "sources": {"layernorm.cu": "e66f36105992687b", "common.cuh": "c9dc0987f95761ca"}},
+    "mlp_up": {"bytes": 16.18e6, "kernel": "mlp_up_kernel",
+               "sources": {"projections.cu": "e291db50f03adf3f", "common.cuh": "c9dc0987f95761ca"}},
+    "mlp_down": {"bytes": 33.27e6, "kernel": "mlp_down_kernel",
+                 "sources": {"projections.cu": "e291db50f03adf3f", "common.cuh": "c9dc0987f95761ca"}},
 }
 
 WORKLOADS = {
@@ -592,8 +596,10 @@ def run_ours(args):
            "layernorm": {"kernel": "layernorm_kernel", "kernel_ms": mlp_ms["layernorm"],
                          "hbm_gbs": lb / (mlp_ms["layernorm"] / 1e3) / 1e9,
                          "roofline_frac": l_roof / (mlp_ms["layernorm"] / 1e3)},
-           "mlp_up": gemm_rec("mlp_up_kernel", uf, ub, mlp_ms["mlp_up"]),
-           "mlp_down": gemm_rec("mlp_down_kernel", df, db, mlp_ms["mlp_down"]),
+           "mlp_up": dict(gemm_rec("mlp_up_kernel", uf, ub, mlp_ms["mlp_up"]),
+                          traffic=captured_traffic("mlp_up", args.workload)),
+           "mlp_down": dict(gemm_rec("mlp_down_kernel", df, db, mlp_ms["mlp_down"]),
+                            traffic=captured_traffic("mlp_down", args.workload)),
            "note": "y = x + (GELU(g) * u) Wo^T after the MLP's LayerNorm, timed alone over "
                    f"{kp} calls enqueued ahead of the GPU; not part of the step"}
     layer_flops = {k: qf + pf + uf + df + layers[k]["gflop"] * 1e9 for k in ("global", "local")}
