@@ -203,8 +203,9 @@ class Clocks:
 # the CPU oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def time_oracle(wl, rows_global, rows_local, seed=0):
-    """Seconds per query row (all 12 heads) of the fp64 oracle, per kind."""
+def time_oracle(wl, rows_global, rows_local, seed=0, threads=0):
+    """Seconds per query row (all 12 heads) of the fp64 oracle, per kind, on
+    `threads` host threads (0: all)."""
     import oracle
     bits = W.bf16_bits(wl.qkv)
     cu = wl.cu_seqlens.numpy()
@@ -213,9 +214,9 @@ def time_oracle(wl, rows_global, rows_local, seed=0):
         per_seq = max(2, n // max(1, wl.n_seqs))
         rows = W.sample_rows(wl.cu_seqlens, per_seq, seed + (kind == "local"))
         t0 = time.perf_counter()
-        oracle.attention_kind(bits, cu, kind, rows=rows)
+        oracle.attention_kind(bits, cu, kind, rows=rows, threads=threads)
         out[kind] = ((time.perf_counter() - t0) / len(rows), len(rows))
-    return out, oracle.max_threads()
+    return out, (threads if threads > 0 else oracle.max_threads())
 
 
 def cpu_baseline(wl, budget_s=15.0):
@@ -227,10 +228,19 @@ def cpu_baseline(wl, budget_s=15.0):
     nl = int(min(wl.T, max(128, share / max(probe["local"][0], 1e-9))))
     per_row, cores = time_oracle(wl, ng, nl, seed=1)
     sec_per_token = per_row["global"][0] + per_row["local"][0]
+    # the same oracle on one host thread, on a sample of about budget_s / 4
+    # seconds (a row on one thread costs about `cores` times its share above)
+    ng1 = int(min(wl.T, max(8, share / 4 / max(per_row["global"][0] * cores, 1e-9))))
+    nl1 = int(min(wl.T, max(64, share / 4 / max(per_row["local"][0] * cores, 1e-9))))
+    one, _ = time_oracle(wl, ng1, nl1, seed=2, threads=1)
+    sec_one = one["global"][0] + one["local"][0]
     return {"value": 1.0 / sec_per_token, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": (f"fp64 oracle, {per_row['global'][1]} sampled query rows of the global "
                        f"layer and {per_row['local'][1]} of the local layer (all 12 heads), "
-                       f"time per row extrapolated to {wl.T} tokens")}
+                       f"time per row extrapolated to {wl.T} tokens"),
+            "one_thread": {"value": 1.0 / sec_one, "unit": UNIT, "cores": 1,
+                           "sample": (f"{one['global'][1]} global and {one['local'][1]} local "
+                                      "sampled query rows on one host thread")}}
 
 
 # ---------------------------------------------------------------------------
