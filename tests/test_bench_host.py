@@ -35,6 +35,23 @@ def test_work_of_the_headline_workload():
     assert g["bytes"] == l["bytes"] == 8192 * 6144
 
 
+def test_work_of_the_22_layer_schedule():
+    """32 sequences of 8192 tokens, layer i global iff i % 3 == 0: 8 global
+    layers of 6.597 TFLOP and 14 local ones of 0.1035 TFLOP, 54.23 TFLOP in
+    all; 1.611 GB per layer (qkv read once, out written once)."""
+    from encoder_only_transformer_gb300 import workloads as W
+    lengths = [8192] * 32
+    kinds = [W.layer_kind(i) for i in range(22)]
+    assert kinds.count("global") == 8 and kinds.count("local") == 14
+    assert kinds[0] == "global" and kinds[1] == kinds[2] == "local"
+    g, l = bench.work(lengths, "global"), bench.work(lengths, "local")
+    assert g["flops"] == 32 * 8192 * 8192 * 256 * 12
+    assert l["flops"] == 32 * (129 * 8192 - 64 * 65) * 256 * 12
+    assert g["bytes"] == l["bytes"] == 32 * 8192 * 6144
+    total = sum(bench.work(lengths, k)["flops"] for k in kinds)
+    assert abs(total / 1e12 - 54.2252) < 1e-3
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
