@@ -255,7 +255,8 @@ int oracle_sdpa_dense(const double *Q, const double *K, const double *V,
 /* ------------------------------------------------------------------ */
 
 /* Per (sequence, head) working state: rotated keys, computed on first use
- * and reused by every query of the task, and the value rows in fp64. */
+ * and reused by every query of that (sequence, head), and the value rows
+ * in fp64. */
 struct seq_ctx {
     const uint16_t *qkv;
     int64_t row0;          /* packed row of position 0 */
