@@ -84,3 +84,24 @@ def test_max_over_ranks_gloo_world2():
     res = sorted(q.get() for _ in range(2))
     assert all(r[1] == 15.0 for r in res)
     assert all(abs(r[2] - 2 * 8192 / 0.015) < 1e-6 for r in res)
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the keys the benchmark contract asks of that arm."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--cpu-budget", "0.25"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference"
+    assert rec["metric"] == bench.METRIC and rec["unit"] == bench.UNIT
+    assert rec["higher_is_better"] is True and rec["steps"] == 1 and rec["warmup"] == 3
+    assert rec["value"] > 0 and rec["cpu_baseline"]["value"] == rec["value"]
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
+    assert rec["e2e"] == {"value": rec["value"], "unit": rec["unit"],
+                          "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
