@@ -55,6 +55,14 @@ def lib():
                                        ctypes.c_int, ctypes.c_double, ctypes.c_int, i64p,
                                        ctypes.c_int64, dp, i32p, ctypes.c_int]
         L.oracle_attention.restype = ctypes.c_int
+        L.oracle_attention_rounded.argtypes = L.oracle_attention.argtypes
+        L.oracle_attention_rounded.restype = ctypes.c_int
+        L.oracle_round_bf16.argtypes = [ctypes.c_double]
+        L.oracle_round_bf16.restype = ctypes.c_double
+        L.oracle_round_bf16_n.argtypes = [dp, ctypes.c_int64, dp]
+        L.oracle_round_bf16_n.restype = None
+        L.oracle_rope_rows.argtypes = [dp, ctypes.c_int64, i64p, ctypes.c_double, ctypes.c_int, dp]
+        L.oracle_rope_rows.restype = None
         L.oracle_out_proj.argtypes = [u16p, u16p, u16p, ctypes.c_int64, ctypes.c_int, i64p,
                                       ctypes.c_int64, dp, ctypes.c_int]
         L.oracle_out_proj.restype = ctypes.c_int
@@ -98,6 +106,17 @@ def rope(x, pos: int, theta: float) -> np.ndarray:
     return y
 
 
+def rope_rows(x, pos, theta: float) -> np.ndarray:
+    """Rotate rows x[n, head_dim] (fp64), row r sitting at position pos[r]."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    p = np.ascontiguousarray(pos, dtype=np.int64)
+    assert x.ndim == 2 and p.shape == (x.shape[0],)
+    y = np.empty_like(x)
+    lib().oracle_rope_rows(_ptr(x, ctypes.c_double), x.shape[0], _ptr(p, ctypes.c_int64),
+                           float(theta), x.shape[1], _ptr(y, ctypes.c_double))
+    return y
+
+
 def key_counts(cu_seqlens, half_window: int) -> np.ndarray:
     """|A_i| of every packed row, by brute force over the band predicate."""
     cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
@@ -133,14 +152,26 @@ def sdpa_dense(Q, K, V, scale: float, mask=None):
     return w, o
 
 
+def round_bf16(x) -> np.ndarray:
+    """Each value rounded to the nearest bf16 (8 significant bits, ties to
+    even), as fp64."""
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(a)
+    lib().oracle_round_bf16_n(_ptr(a, ctypes.c_double), a.size, _ptr(y, ctypes.c_double))
+    return y
+
+
 def attention(qkv_bits, cu_seqlens, theta: float, half_window: int, rows=None,
-              threads: int = 0, heads: int = HEADS, head_dim: int = HEAD_DIM):
+              threads: int = 0, heads: int = HEADS, head_dim: int = HEAD_DIM,
+              round_operands: bool = False):
     """The attention block in fp64.
 
     qkv_bits: uint16 [T, 3*heads*head_dim], the bf16 bit patterns of the fused
     Wqkv output.  cu_seqlens: int32 [n_seqs+1].  rows: None (every row) or a
     sorted array of packed row indices.  Returns (out fp64 [n, heads*head_dim],
-    counts int32 [n]).
+    counts int32 [n]).  round_operands: round the rotated q and k rows to bf16
+    before forming the scores (the operands a bf16 tensor-core path
+    multiplies); everything else stays fp64.
     """
     q = np.ascontiguousarray(qkv_bits)
     if q.dtype != np.uint16:
@@ -157,10 +188,10 @@ def attention(qkv_bits, cu_seqlens, theta: float, half_window: int, rows=None,
         rp = _ptr(r, ctypes.c_int64)
     out = np.empty((n, heads * head_dim), dtype=np.float64)
     counts = np.zeros(n, dtype=np.int32)
-    rc = lib().oracle_attention(_ptr(q, ctypes.c_uint16), T, heads, head_dim,
-                                _ptr(cu, ctypes.c_int32), len(cu) - 1, float(theta),
-                                int(half_window), rp, n, _ptr(out, ctypes.c_double),
-                                _ptr(counts, ctypes.c_int32), int(threads))
+    fn = lib().oracle_attention_rounded if round_operands else lib().oracle_attention
+    rc = fn(_ptr(q, ctypes.c_uint16), T, heads, head_dim, _ptr(cu, ctypes.c_int32),
+            len(cu) - 1, float(theta), int(half_window), rp, n, _ptr(out, ctypes.c_double),
+            _ptr(counts, ctypes.c_int32), int(threads))
     if rc:
         raise ValueError(f"oracle_attention failed (code {rc})")
     return out, counts
@@ -335,8 +366,9 @@ def attention_padded(qkv_bits, mask, theta: float, half_window: int,
     return out
 
 
-def attention_kind(qkv_bits, cu_seqlens, kind: str, rows=None, threads: int = 0):
+def attention_kind(qkv_bits, cu_seqlens, kind: str, rows=None, threads: int = 0,
+                   round_operands: bool = False):
     """attention() with the constants of a ModernBERT-base layer kind."""
     p = KINDS[kind]
     return attention(qkv_bits, cu_seqlens, p["theta"], p["half_window"], rows=rows,
-                     threads=threads)
+                     threads=threads, round_operands=round_operands)

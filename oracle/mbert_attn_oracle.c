@@ -30,7 +30,7 @@
  *    the softmax, so real outputs are unchanged.  Here every packed sequence
  *    is its own attention problem; keys of other sequences are never seen.
  *
- * Readings where the pages are silent (each one is listed in the design doc):
+ * Readings where the pages are silent:
  *  - rotation sign: y = x*cos(phi) + rotate_half(x)*sin(phi) with
  *    rotate_half(x) = (-x[32..63], x[0..31]), i.e. pair m = (x[m], x[m+32])
  *    is multiplied by exp(+i*phi) when read as the complex number
@@ -63,6 +63,27 @@ static double bf16_to_f64(uint16_t bits)
     return (double)f;
 }
 
+/* Round x to the nearest bf16 value (8 significant bits), ties to even.
+ * frexp gives x = m * 2^e with 0.5 <= |m| < 1; m * 2^8 rounded to an integer
+ * (nearbyint, the default round-to-nearest-even mode) keeps 8 significant
+ * bits.  Zero, infinities and NaN pass through; the bf16 overflow and
+ * subnormal ranges are not modelled (no input here reaches them). */
+double oracle_round_bf16(double x)
+{
+    if (x == 0.0 || !isfinite(x))
+        return x;
+    int e;
+    double m = frexp(x, &e);
+    return ldexp(nearbyint(ldexp(m, 8)), e - 8);
+}
+
+/* oracle_round_bf16 over n values. */
+void oracle_round_bf16_n(const double *x, int64_t n, double *y)
+{
+    for (int64_t i = 0; i < n; i++)
+        y[i] = oracle_round_bf16(x[i]);
+}
+
 /* ------------------------------------------------------------------ */
 /* RoPE                                                                */
 /* ------------------------------------------------------------------ */
@@ -90,6 +111,14 @@ void oracle_rope_row(const double *x, int64_t pos, double theta, int head_dim,
         y[m] = a * c - b * s;
         y[m + half] = b * c + a * s;
     }
+}
+
+/* oracle_rope_row over n rows x[n][head_dim], row r at position pos[r]. */
+void oracle_rope_rows(const double *x, int64_t n, const int64_t *pos, double theta,
+                      int head_dim, double *y)
+{
+    for (int64_t r = 0; r < n; r++)
+        oracle_rope_row(x + r * head_dim, pos[r], theta, head_dim, y + r * head_dim);
 }
 
 /* ------------------------------------------------------------------ */
@@ -264,6 +293,7 @@ struct seq_ctx {
     int width;             /* 3 * heads * head_dim */
     int heads, head_dim, h;
     double theta;
+    int round_operands;    /* rotated q and k rounded to bf16 (see below) */
     double *krot;          /* [L][head_dim] */
     unsigned char *kdone;  /* [L] */
     double *vbuf;          /* [L][head_dim] */
@@ -294,6 +324,9 @@ static const double *seq_krot(struct seq_ctx *c, int64_t j)
         for (int e = 0; e < c->head_dim; e++)
             raw[e] = bf16_to_f64(src[e]);
         oracle_rope_row(raw, j, c->theta, c->head_dim, k);
+        if (c->round_operands)
+            for (int e = 0; e < c->head_dim; e++)
+                k[e] = oracle_round_bf16(k[e]);
         c->kdone[j] = 1;
     }
     return k;
@@ -324,10 +357,10 @@ struct task { int s, h; int64_t r0, r1; };  /* requested-row index range */
  * threads: OpenMP threads to use (<= 0: the runtime default).
  * Returns 0, or a negative code for bad arguments.
  */
-int oracle_attention(const uint16_t *qkv, int64_t T, int heads, int head_dim,
-                     const int32_t *cu, int n_seqs, double theta,
-                     int half_window, const int64_t *rows, int64_t n_rows,
-                     double *out, int32_t *counts, int threads)
+static int attention_impl(const uint16_t *qkv, int64_t T, int heads, int head_dim,
+                          const int32_t *cu, int n_seqs, double theta,
+                          int half_window, const int64_t *rows, int64_t n_rows,
+                          double *out, int32_t *counts, int threads, int round_operands)
 {
     if (!qkv && T > 0)
         return -10;
@@ -390,6 +423,7 @@ int oracle_attention(const uint16_t *qkv, int64_t T, int heads, int head_dim,
         struct seq_ctx c;
         c.qkv = qkv; c.row0 = row0; c.L = L; c.width = width;
         c.heads = heads; c.head_dim = head_dim; c.h = tk->h; c.theta = theta;
+        c.round_operands = round_operands;
         c.krot = (double *)malloc(sizeof(double) * (size_t)(L * head_dim));
         c.vbuf = (double *)malloc(sizeof(double) * (size_t)(L * head_dim));
         c.kdone = (unsigned char *)calloc((size_t)L, 1);
@@ -410,6 +444,9 @@ int oracle_attention(const uint16_t *qkv, int64_t T, int heads, int head_dim,
             for (int e = 0; e < head_dim; e++)
                 qraw[e] = bf16_to_f64(qsrc[e]);
             oracle_rope_row(qraw, i, theta, head_dim, qrot);
+            if (round_operands)
+                for (int e = 0; e < head_dim; e++)
+                    qrot[e] = oracle_round_bf16(qrot[e]);
 
             int64_t j0, j1;
             admitted_range(i, L, half_window, &j0, &j1);
@@ -430,6 +467,32 @@ int oracle_attention(const uint16_t *qkv, int64_t T, int heads, int head_dim,
     }
     free(tasks);
     return failed ? -20 : 0;
+}
+
+int oracle_attention(const uint16_t *qkv, int64_t T, int heads, int head_dim,
+                     const int32_t *cu, int n_seqs, double theta,
+                     int half_window, const int64_t *rows, int64_t n_rows,
+                     double *out, int32_t *counts, int threads)
+{
+    return attention_impl(qkv, T, heads, head_dim, cu, n_seqs, theta, half_window,
+                          rows, n_rows, out, counts, threads, 0);
+}
+
+/* The same block with the rotated q and k rows rounded to bf16 before the
+ * scores are formed, everything else in fp64.  A tensor-core path multiplies
+ * bf16 operands, so the rotated rows it multiplies are these rounded rows
+ * (the reading of the intermediates' precision); with scores spread over
+ * tens of units that rounding alone moves the weights of near-tied keys by
+ * more than the output tolerance, while the rest of the computation (the
+ * softmax, its rescaling and the blend) is still checked at full tolerance
+ * against this variant. */
+int oracle_attention_rounded(const uint16_t *qkv, int64_t T, int heads, int head_dim,
+                             const int32_t *cu, int n_seqs, double theta,
+                             int half_window, const int64_t *rows, int64_t n_rows,
+                             double *out, int32_t *counts, int threads)
+{
+    return attention_impl(qkv, T, heads, head_dim, cu, n_seqs, theta, half_window,
+                          rows, n_rows, out, counts, threads, 1);
 }
 
 int oracle_max_threads(void);

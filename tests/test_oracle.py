@@ -171,6 +171,16 @@ def test_rope_matches_complex_multiplication():
             np.testing.assert_allclose(oracle.rope(x[r], p, theta), ref[r], rtol=0, atol=1e-12)
 
 
+def test_rope_rows_equal_row_by_row():
+    """The many-rows form rotates each row exactly as the one-row form."""
+    g = np.random.default_rng(8)
+    x = g.standard_normal((50, 64))
+    pos = g.integers(0, 8192, 50)
+    y = oracle.rope_rows(x, pos, 160000.0)
+    for r in range(50):
+        np.testing.assert_array_equal(y[r], oracle.rope(x[r], int(pos[r]), 160000.0))
+
+
 def test_rope_relative_position_and_norm():
     """Teardown: after RoPE the score depends on how far apart the two
     tokens are.  q(m).k(n) == q(m+t).k(n+t); each pair keeps its length;
@@ -252,6 +262,89 @@ def test_attention_matches_bruteforce(lengths, kind):
     np.testing.assert_allclose(out, ref_np, rtol=0, atol=1e-12)
     np.testing.assert_allclose(out, ref_t, rtol=0, atol=1e-12)
     np.testing.assert_array_equal(counts, oracle.key_counts(wl.cu_seqlens.numpy(), p["half_window"]))
+
+
+# ---------------------------------------------------------------------------
+# the rotated operands rounded to bf16 (what a bf16 tensor-core path
+# multiplies): the rounding itself and the block computed on rounded operands
+# ---------------------------------------------------------------------------
+
+def _round_bf16_bits(x):
+    """Round fp64 values to 8 significant bits, ties to even, by bit
+    manipulation of the binary64 encoding: keep the top 7 of the 52 stored
+    fraction bits, then add one unit of the kept last place when the dropped
+    part is above half of it, or exactly half with an odd kept part."""
+    x = np.asarray(x, dtype=np.float64)
+    u = x.view(np.uint64).copy()
+    drop = np.uint64(45)
+    low = u & ((np.uint64(1) << drop) - np.uint64(1))
+    half = np.uint64(1) << (drop - np.uint64(1))
+    kept = u & ~((np.uint64(1) << drop) - np.uint64(1))
+    odd = (kept >> drop) & np.uint64(1)
+    up = (low > half) | ((low == half) & (odd == np.uint64(1)))
+    kept = kept + np.where(up, np.uint64(1) << drop, np.uint64(0)).astype(np.uint64)
+    out = kept.view(np.float64)
+    return np.where(x == 0, x, out)
+
+
+def test_round_bf16_matches_torch_and_bit_rounding():
+    """oracle.round_bf16 against torch's fp32 -> bf16 conversion on values
+    that fp32 holds exactly, against the bit-level rounding on arbitrary fp64
+    values, and on exact midpoints (ties go to the even neighbour)."""
+    g = np.random.default_rng(5)
+    x32 = (g.standard_normal(20000) * np.exp(g.uniform(-20, 20, 20000))).astype(np.float32)
+    x = x32.astype(np.float64)
+    ref = torch.from_numpy(x32).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(x), ref)
+    y = g.standard_normal(20000) * np.exp(g.uniform(-20, 20, 20000))
+    np.testing.assert_array_equal(oracle.round_bf16(y), _round_bf16_bits(y))
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 3 * 2.0 ** -9 + 2.0 ** -17])
+    np.testing.assert_array_equal(oracle.round_bf16(ties)[:3], [1.0, 1 + 2.0 ** -6, -1.0])
+    assert oracle.round_bf16(ties)[3] == _round_bf16_bits(ties)[3]
+
+
+@pytest.mark.parametrize("lengths", [[5, 64, 65], [130, 7, 200]], ids=str)
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_rounded_operands_match_bruteforce(lengths, kind):
+    """The block on rounded operands: complex-number RoPE in numpy, the
+    bit-level rounding above on the rotated q and k, dense scores / 8 with an
+    explicit band mask, softmax and blend.  Inputs of spread 4 (scores of
+    spread ~16) make the rounding matter: the result differs from the
+    unrounded block, yet equals the brute force to 1e-12."""
+    wl = W.custom(lengths, seed=sum(lengths) + 17, sigma=4.0)
+    p = oracle.KINDS[kind]
+    out, _ = oracle.attention(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), p["theta"],
+                              p["half_window"], round_operands=True)
+    q, k, v = _heads_view(wl.qkv)
+    ref = np.zeros((wl.T, 768))
+    cu = wl.cu_seqlens.tolist()
+    for s in range(len(cu) - 1):
+        b, e = cu[s], cu[s + 1]
+        pos = np.arange(e - b)
+        mask = _band_mask(e - b, p["half_window"])
+        for h in range(12):
+            qr = _round_bf16_bits(_rope_complex(q[b:e, h], pos, p["theta"]))
+            kr = _round_bf16_bits(_rope_complex(k[b:e, h], pos, p["theta"]))
+            sc = np.where(mask, qr @ kr.T / 8.0, -np.inf)
+            w = np.exp(sc - sc.max(axis=1, keepdims=True))
+            w /= w.sum(axis=1, keepdims=True)
+            ref[b:e, h * 64:(h + 1) * 64] = w @ v[b:e, h]
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    plain, _ = oracle.attention(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), p["theta"],
+                                p["half_window"])
+    assert np.abs(plain - out).max() > 1e-3
+
+
+def test_rounded_operands_at_position_zero_are_exact():
+    """At position 0 RoPE turns nothing, so the rotated rows are the bf16
+    inputs themselves and rounding them changes nothing: a pack of length-1
+    sequences gives bit-identical results with and without the rounding."""
+    wl = W.custom([1, 1, 1, 1, 1], seed=23, sigma=4.0)
+    for kind in ("global", "local"):
+        a, _ = oracle.attention_kind(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), kind)
+        b, _ = oracle.attention_kind(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), kind,
+                                     round_operands=True)
+        np.testing.assert_array_equal(a, b)
 
 
 def test_wrong_theta_or_window_is_detected():

@@ -50,6 +50,12 @@ PLANTS = [
     ("gelu_tanh_form", "return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));",
      "return 0.5 * z * (1.0 + tanh(sqrt(2.0 / 3.14159265358979323846) * (z + 0.044715 * z * z * z)));"),
     ("mlp_halves_swapped", "m[j] = gelu_erf(g) * u;", "m[j] = gelu_erf(u) * g;"),
+    ("round_bf16_seven_bits", "return ldexp(nearbyint(ldexp(m, 8)), e - 8);",
+     "return ldexp(nearbyint(ldexp(m, 7)), e - 7);"),
+    ("round_bf16_truncates", "return ldexp(nearbyint(ldexp(m, 8)), e - 8);",
+     "return ldexp(trunc(ldexp(m, 8)), e - 8);"),
+    ("rounded_keys_not_rounded", "        if (c->round_operands)\n            for (int e = 0; e < c->head_dim; e++)\n                k[e] = oracle_round_bf16(k[e]);\n",
+     ""),
     ("mlp_without_residual", "y[k * d + o] = bf16_to_f64(x[t * d + o]) + acc;\n        }\n        free(h);",
      "y[k * d + o] = acc;\n        }\n        free(h);"),
 ]
@@ -57,7 +63,8 @@ PLANTS = [
 # every exported function whose ctypes signature the copies must share
 _FUNCS = ("oracle_inv_freq", "oracle_rope_row", "oracle_key_counts", "oracle_sdpa_dense",
           "oracle_attention", "oracle_out_proj", "oracle_layernorm", "oracle_ln_qkv",
-          "oracle_gelu", "oracle_mlp", "oracle_max_threads")
+          "oracle_gelu", "oracle_mlp", "oracle_max_threads", "oracle_attention_rounded",
+          "oracle_round_bf16", "oracle_round_bf16_n", "oracle_rope_rows")
 
 
 def _pins():
@@ -85,6 +92,10 @@ def _pins():
     out += [M.test_gelu_printed_values, M.test_gelu_matches_torch_exact_form,
             M.test_zero_down_projection_returns_the_residual,
             M.test_selection_weights_give_gelu_times_gate, M.test_matches_library_composition]
+    out += [T.test_round_bf16_matches_torch_and_bit_rounding,
+            T.test_rounded_operands_at_position_zero_are_exact]
+    out += [(lambda lengths=lengths, kind=kind: T.test_rounded_operands_match_bruteforce(lengths, kind))
+            for lengths in ([5, 64, 65],) for kind in ("global", "local")]
     out += [(lambda r=r: T.test_key_counts_match_pages(r)) for r in table]
     for lengths in ([5, 64, 65], [130, 7, 200]):
         for kind in ("global", "local"):
