@@ -253,15 +253,10 @@ attn_generic_kernel(const __grid_constant__ CUtensorMap tm_rot,
 
 cudaError_t launch_attn_generic(const AttnArgs &a, cudaStream_t stream)
 {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_generic_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess)
-            return e;
-        configured = true;
-    }
+    static PerDeviceOnce smem_once;
+    cudaError_t e = smem_opt_in(smem_once, attn_generic_kernel, kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
     const long long grid = static_cast<long long>(a.entry_bound) * kHeads;
     return launch_chained(attn_generic_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, stream,
         a.tm_rot, a.tm_qkv, a.cu, a.work, a.work_count, a.half_window, a.out, a.err);

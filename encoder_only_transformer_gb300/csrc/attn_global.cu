@@ -601,17 +601,10 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
 
 cudaError_t launch_attn_global(const AttnArgs &a, cudaStream_t stream)
 {
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_global_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = true;
-    }
+    static PerDeviceOnce smem_once;
+    cudaError_t e = smem_opt_in(smem_once, attn_global_kernel, kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
     return launch_chained(attn_global_kernel, dim3(a.num_ctas), dim3(kThreads), kSmemBytes, stream,
         a.tm_rot, a.tm_qkv, a.cu, a.work, a.work_count, a.tile_start, a.unit_cnt, a.partials,
         a.out, a.err);

@@ -779,8 +779,8 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
             // 2^(s * scale - m) is then written chunk by chunk in one pass.
             // Any reference within 2^kSlack of the row maximum gives the
             // same softmax up to rounding; a chunk whose exponents exceed
-            // kSlack raises m and rescales the P already written (exact
-            // powers of two).
+            // kSlack raises m by an integer and rescales the P already
+            // written by that power of two (exact in bf16).
             uint32_t v[32];
             tmem_ld32(tm + 32 * (q + 2), v);
             tmem_wait_ld();
@@ -835,11 +835,16 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
                 }
                 const float ymax = max32(v);
                 if (__any_sync(0xffffffffu, ymax > kSlack)) {
-                    // raise m by d (0 in lanes that need no change) and
-                    // rescale this chunk's exponents, the P already written
-                    // and the sums by 2^-d
-                    const float d = ymax > kSlack ? ymax : 0.f;
-                    const float f = ex2_approx(-d);
+                    // raise m by the integer d = ceil(ymax) (0 in lanes that
+                    // need no change) and rescale this chunk's exponents, the
+                    // P already written and the sums by f = 2^-d, built from
+                    // its exponent bits: multiplying a bf16 P by f is exact,
+                    // so nothing already written is rounded again.  Past
+                    // d = 126 the scaled P would be below 2^-62 of the new
+                    // maximum; it is flushed to 0.
+                    const float d = ymax > kSlack ? fminf(ceilf(ymax), 1024.f) : 0.f;
+                    const int di = static_cast<int>(d);
+                    const float f = di <= 126 ? __int_as_float((127 - di) << 23) : 0.f;
                     tmem_wait_st();
 #pragma unroll 1
                     for (int e2 = 0; e2 < e; ++e2) {
@@ -913,17 +918,10 @@ attn_local_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_const
 
 cudaError_t launch_attn_local(const LocalArgs &a, cudaStream_t stream)
 {
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_local_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = true;
-    }
+    static PerDeviceOnce smem_once;
+    cudaError_t e = smem_opt_in(smem_once, attn_local_kernel, kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
     const long long units = static_cast<long long>(a.block_bound) * kHeads;
     const long long grid = units < a.num_ctas ? units : a.num_ctas;
     if (grid <= 0)

@@ -7,7 +7,62 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace mbert {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device set-up of one kernel that must happen once in each device
+// context before its first launch there (a shared-memory opt-in, an
+// occupancy query).  Safe to use from several host threads: the first
+// caller on a device runs the set-up under the lock, later callers read the
+// published value without locking.
+struct PerDeviceOnce {
+    std::mutex mu;
+    std::atomic<int> value[kMaxDevices] = {};   // 0: not set up yet
+};
+
+// Returns in *value the set-up result for the current device (a positive
+// int), running `setup(&v)` on the first call there.
+template <typename Setup>
+cudaError_t per_device_once(PerDeviceOnce &once, int *value, Setup setup)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    int v = once.value[dev].load(std::memory_order_acquire);
+    if (v == 0) {
+        std::lock_guard<std::mutex> lock(once.mu);
+        v = once.value[dev].load(std::memory_order_relaxed);
+        if (v == 0) {
+            e = setup(&v);
+            if (e != cudaSuccess)
+                return e;
+            once.value[dev].store(v, std::memory_order_release);
+        }
+    }
+    *value = v;
+    return cudaSuccess;
+}
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device (once per device).
+template <typename Kernel>
+cudaError_t smem_opt_in(PerDeviceOnce &once, Kernel kernel, size_t bytes)
+{
+    int v = 0;
+    return per_device_once(once, &v, [&](int *out) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(bytes));
+        *out = 1;
+        return e;
+    });
+}
 
 // Launch `kernel` on `stream` with programmatic stream serialization: its
 // launch may overlap the tail of the previous kernel in the stream, which

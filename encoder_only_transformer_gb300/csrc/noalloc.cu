@@ -5,16 +5,29 @@
 // process whose memory is reserved up front and must not grow afterwards,
 // or a real-time loop that cannot afford the device-wide synchronisation a
 // cudaMalloc or cudaFree may cause.  They cannot create a handle (creating
-// one allocates the RoPE tables and the workspace), so this entry point runs
-// the same kernels as mbert_attn_forward with every piece of scratch memory
-// (work list, work count, error word, rotated Q/K rows and the two RoPE
-// tables) carved out of one file-scope static __device__ array.
+// one allocates the RoPE tables and the workspace), so this entry point
+// takes every piece of scratch memory (work list, work count, error word,
+// rotated Q/K rows and the two RoPE tables) from one file-scope static
+// __device__ array.
+//
+// It is not the benchmarked path: for both layer kinds it runs the plan
+// kernel, the RoPE pass into the static rotated-Q/K rows and the generic
+// attention kernel (one CTA per 128-query block and head), not the
+// persistent global and local kernels of mbert_attn_forward.  Its results
+// agree with the oracle within the same bounds; its speed and its fp32
+// summation order differ.
 //
 // That array lives in every GPU context that loads this part of the
 // library, from the first call on that device until the process exits.
 // All calls share it and it keeps the last call's contents: each call
 // clears the words that must start at zero, and two calls whose work
 // overlaps on the GPU (for example on two streams) race on it.
+//
+// The first call on a device sets up that device: it looks up the array's
+// device address and fills the RoPE tables with a blocking copy, which
+// synchronises with other work on the device.  Make that first call before
+// any stream capture and outside any loop that must not block; later calls
+// only enqueue work on the caller's stream.
 #include <cmath>
 #include <mutex>
 
@@ -52,7 +65,6 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-constexpr int kMaxDevices = 64;
 struct DeviceState {
     bool ready = false;
     unsigned char *base = nullptr;   // device address of g_scratch on this device

@@ -529,30 +529,28 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 }
 
 // Pairs of CTAs to launch for `kernel`: as many as fit at once (per device,
-// found once), at most one per unit.  Sets the shared-memory opt-in.
+// found once, with the shared-memory opt-in set first), at most one per unit.
 template <typename Kernel>
-cudaError_t pair_count(Kernel kernel, int (&cache)[64], int num_ctas, long long n_units, int *pairs)
+cudaError_t pair_count(Kernel kernel, PerDeviceOnce &once, int num_ctas, long long n_units, int *pairs)
 {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64)
-        return cudaErrorInvalidDevice;
-    if (cache[dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    int fit = 0;
+    cudaError_t e = per_device_once(once, &fit, [&](int *out) {
+        cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess)
-            return e;
+        if (r != cudaSuccess)
+            return r;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (num_ctas / 2));
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = kSmemBytes;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-        if (e != cudaSuccess)
-            return e;
-        cache[dev] = n > 0 ? n : 1;
-    }
-    *pairs = static_cast<int>(n_units < cache[dev] ? n_units : cache[dev]);   // >= 1 unit each
+        r = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+        *out = n > 0 ? n : 1;
+        return r;
+    });
+    if (e != cudaSuccess)
+        return e;
+    *pairs = static_cast<int>(n_units < fit ? n_units : fit);   // >= 1 unit each
     return cudaSuccess;
 }
 
@@ -560,7 +558,7 @@ cudaError_t pair_count(Kernel kernel, int (&cache)[64], int num_ctas, long long 
 
 cudaError_t launch_out_proj(const OutProjArgs &a, cudaStream_t stream)
 {
-    static int max_pairs[64] = {};
+    static PerDeviceOnce max_pairs;
     const long long n_units = ((a.T + kUnitM - 1) / kUnitM) * (kHidden / kBN);
     if (n_units <= 0)
         return cudaSuccess;
@@ -574,7 +572,7 @@ cudaError_t launch_out_proj(const OutProjArgs &a, cudaStream_t stream)
 
 cudaError_t launch_mlp_down(const OutProjArgs &a, cudaStream_t stream)
 {
-    static int max_pairs[64] = {};
+    static PerDeviceOnce max_pairs;
     const long long n_units = ((a.T + kUnitM - 1) / kUnitM) * (kHidden / kBN);
     if (n_units <= 0)
         return cudaSuccess;
@@ -588,7 +586,7 @@ cudaError_t launch_mlp_down(const OutProjArgs &a, cudaStream_t stream)
 
 cudaError_t launch_qkv_proj(const QkvProjArgs &a, cudaStream_t stream)
 {
-    static int max_pairs[64] = {};
+    static PerDeviceOnce max_pairs;
     const long long n_units = ((a.T + kUnitM - 1) / kUnitM) * (kQKVWidth / kBN);
     if (n_units <= 0)
         return cudaSuccess;
@@ -602,7 +600,7 @@ cudaError_t launch_qkv_proj(const QkvProjArgs &a, cudaStream_t stream)
 
 cudaError_t launch_mlp_up(const QkvProjArgs &a, cudaStream_t stream)
 {
-    static int max_pairs[64] = {};
+    static PerDeviceOnce max_pairs;
     const long long n_units = ((a.T + kUnitM - 1) / kUnitM) * (kInner / (kBN / 2));
     if (n_units <= 0)
         return cudaSuccess;

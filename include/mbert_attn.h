@@ -250,10 +250,18 @@ int mbert_attn_selftest_timeout(mbert_attn *h, int64_t limit_us, void *stream);
  * MBERT_NOALLOC_MAX_TOKENS, or max_seqlen above it, are rejected
  * (MBERT_ERR_BAD_ARG / MBERT_ERR_SEQ_TOO_LONG) before anything is enqueued.
  * The first call on a device does a one-time set-up (it looks up the
- * array's device address and fills the RoPE tables with synchronous
- * copies); make that first call before any stream capture.  Every call
- * shares the array and overwrites what the previous call left there, so two
- * calls whose work overlaps on the GPU (e.g. on different streams) race. */
+ * array's device address and fills the RoPE tables with blocking copies,
+ * which synchronise with other work on that device); make that first call
+ * before any stream capture and outside any loop that must not block.
+ * Every call shares the array and overwrites what the previous call left
+ * there, so two calls whose work overlaps on the GPU (e.g. on different
+ * streams) race.
+ * This is not the benchmarked path: for both layer kinds it runs the plan
+ * kernel, a RoPE pass into the static rotated-Q/K rows and the generic
+ * attention kernel (one CTA per 128-query block and head), not the
+ * persistent kernels of mbert_attn_forward, so its speed and its fp32
+ * summation order differ; its results meet the same bounds against the
+ * oracle. */
 int mbert_attn_forward_noalloc(const void *qkv, const int32_t *cu_seqlens, int n_seqs,
                                int64_t total_tokens, int max_seqlen, int layer_kind,
                                void *out, int32_t *device_status, void *stream);
