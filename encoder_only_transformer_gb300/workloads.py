@@ -52,20 +52,55 @@ def cu_from_lengths(lengths) -> torch.Tensor:
     return torch.tensor(cu, dtype=torch.int32)
 
 
-def draw_qkv(g: torch.Generator, T: int, sigma: float) -> torch.Tensor:
+def draw_qkv(g: torch.Generator, T: int, sigma: float, sigma_qk: Optional[float] = None) -> torch.Tensor:
+    """randn(T, 2304) * sigma rounded to bf16; with sigma_qk the Q and K
+    columns (0 .. 1535) are drawn with that spread instead, V keeping sigma."""
     x = torch.randn(T, WIDTH, generator=g, dtype=torch.float32)
     if sigma != 1.0:
         x.mul_(sigma)
+    if sigma_qk is not None:
+        x[:, :2 * OUT_WIDTH].mul_(sigma_qk / sigma)
     return x.to(torch.bfloat16)
 
 
 def custom(lengths, seed: int, sigma: float = 1.0, kinds=("global", "local"),
-           name: Optional[str] = None) -> Workload:
+           name: Optional[str] = None, sigma_qk: Optional[float] = None) -> Workload:
     g = torch.Generator().manual_seed(seed)
     lengths = [int(L) for L in lengths]
     cu = cu_from_lengths(lengths)
-    qkv = draw_qkv(g, int(cu[-1]), sigma)
+    qkv = draw_qkv(g, int(cu[-1]), sigma, sigma_qk)
     return Workload(name or f"custom{lengths}", seed, sigma, lengths, list(kinds), qkv, cu)
+
+
+def spiked(lengths, seed: int, every: int, factor: float) -> Workload:
+    """N(0, 1) rows whose K columns (768 .. 1535, every head) are multiplied
+    by `factor` on every `every`-th packed row: a few keys whose scores are
+    far above (or below) the rest for many queries."""
+    g = torch.Generator().manual_seed(seed)
+    lengths = [int(L) for L in lengths]
+    cu = cu_from_lengths(lengths)
+    T = int(cu[-1])
+    x = torch.randn(T, WIDTH, generator=g, dtype=torch.float32)
+    x[::every, OUT_WIDTH:2 * OUT_WIDTH].mul_(factor)
+    return Workload(f"spiked{lengths}x{factor}", seed, 1.0, lengths, ["global", "local"],
+                    x.to(torch.bfloat16), cu)
+
+
+def band_probe(lengths, magnitude: float = 16.0) -> Workload:
+    """Q = K = 0 and, in head h, V[t, h*64 + d] = magnitude when
+    (t + h) % 64 == d, else 0 (t the packed row): no randomness.  Every key
+    puts its magnitude into one column of each head, so a key the softmax
+    admits in error, or leaves out, moves that column of the query's output
+    by about magnitude / (number of admitted keys)."""
+    lengths = [int(L) for L in lengths]
+    cu = cu_from_lengths(lengths)
+    T = int(cu[-1])
+    x = torch.zeros(T, WIDTH, dtype=torch.float32)
+    t = torch.arange(T)
+    for h in range(12):
+        x[t, 2 * OUT_WIDTH + h * 64 + (t + h) % 64] = magnitude
+    return Workload(f"band_probe{lengths}", 0, 0.0, lengths, ["global", "local"],
+                    x.to(torch.bfloat16), cu)
 
 
 def _uniform_lengths(g, n, lo, hi):

@@ -59,6 +59,41 @@ def test_sequence_longer_than_bound(attn):
     assert torch.all(out == 0)
 
 
+# The local kernel validates cu_seqlens itself on two of its paths: one lane
+# per sequence for up to 32 sequences, a warp-wide pass for up to 256; with
+# more sequences the plan kernel checks first.  Each path must report the
+# defect and write nothing.
+LOCAL_PATHS = {"per_lane": 3, "warp_pass": 40, "plan_kernel": 300}
+
+
+@pytest.mark.parametrize("defect", ["decreasing", "first_not_zero", "last_not_total", "too_long"])
+@pytest.mark.parametrize("path", list(LOCAL_PATHS))
+def test_local_layer_device_checks(attn, path, defect):
+    n = LOCAL_PATHS[path]
+    T = 2 * n                                 # n sequences of 2 tokens
+    cu_list = list(range(0, T + 1, 2))
+    max_seqlen = 0
+    if defect == "decreasing":
+        cu_list[n // 2] = cu_list[n // 2 + 1] + 1
+    elif defect == "first_not_zero":
+        cu_list[0] = 1
+    elif defect == "last_not_total":
+        cu_list[-1] = T - 1
+    else:
+        max_seqlen = 1                        # every sequence is longer
+    wl = W.custom([T], seed=4)
+    qkv = wl.qkv.cuda()
+    cu = torch.tensor(cu_list, dtype=torch.int32, device="cuda")
+    out = torch.full((T, 768), 7.0, dtype=torch.bfloat16, device="cuda")
+    rc = _fwd_raw(attn, qkv.data_ptr(), cu, n, T, max_seqlen, 1, out.data_ptr())
+    assert rc == 0
+    assert attn.get_error() == (-3 if defect == "too_long" else -4)
+    assert torch.all(out == 7.0)              # nothing written
+    good = attn.forward(qkv, torch.arange(0, T + 1, 2, dtype=torch.int32, device="cuda"), "local")
+    torch.cuda.synchronize()
+    assert attn.get_error() == 0 and torch.isfinite(good.float()).all()
+
+
 def test_host_checks(attn):
     wl = W.custom([64], seed=3)
     qkv, cu = wl.qkv.cuda(), wl.cu_seqlens.cuda()

@@ -1,0 +1,316 @@
+"""GPU parity where the softmax is hardest: wide score ranges, keys whose
+scores tower over the rest, and the exact edges of the band.
+
+Sources: "ModernBERT-base Architecture Teardown", "How Does Self-Attention
+Work?" (each row of weights sums to 1 over the admitted keys) and "What Are
+Local and Global Attention?" (a local query sees |i - j| <= 64); "ModernBERT"
+(candding), "The alternating attention" (the window is inclusive).
+
+Wide ranges.  With Q and K drawn with spread sigma the scores q.k / 8 spread
+by about sigma^2.  A bf16 tensor-core path multiplies the rotated rows
+rounded to bf16, and at sigma >= 2 that rounding alone moves the weights of
+nearly tied keys by more than the output tolerance, so these tests compare
+against the oracle evaluated on rounded operands
+(oracle.attention(..., round_operands=True), pinned on the CPU).  Two more
+effects of the bf16 arithmetic grow with the spread and get their own
+derived terms in the tolerance of each output element (row i, column c):
+
+* The kernels rotate in fp32; their rotated value lies within eps of the
+  exact one (eps below, from the precision of their cos/sin), so an operand
+  whose exact value sits within eps of a bf16 rounding midpoint may round to
+  the other neighbour, one bf16 step away: a few elements in 10^4, and at
+  these spreads one such step can move a near-tied score by ~0.1.  Term:
+  2 * sum_j w_ij (exp(D_ij) - 1) (|v_jc| + |o_ic|), D_ij the score change if
+  every such operand element of row i and key j took its other rounding (the
+  step times the other operand, / 8); w_ij (v_jc - o_ic) is the first-order
+  effect of a score change, exp(D) - 1 >= D and the factor 2 cover the
+  higher orders and the renormalisation.  It is zero for elements no such
+  operand can reach.
+* P and the output are bf16, each rounded to 8 significant bits (relative
+  error up to 2^-8).  A sharp softmax puts single value rows, up to |v| ~ 4,
+  into the output, where these roundings reach 0.03.  Term:
+  2^-8 * (sum_j w_ij |v_jc| + |o_ic|).
+
+So |err| <= 2e-2 + both terms for every element, and the mean bound (2e-3)
+is unchanged; the tests also check that the operand-rounding term widens
+only a minority of the elements.  What is held to this: the online softmax
+with its rescaling, the blend and the merge of split query blocks.  Each
+test first checks on the CPU that its input reaches the rescaling paths it
+covers.
+
+Band probe.  Q = K = 0 makes every admitted weight exactly 1 / |A_i|, and V
+carries a fixed magnitude in one column per key.  The output is then exact up
+to the final division and bf16 rounding, so it is held to one bf16 rounding
+(2^-8 relative); a single key admitted in error or left out moves an element
+by 16 / (|A_i| + 1), many rounding steps away.  This checks the masks the
+attention kernels apply themselves, not the key-count kernel.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from encoder_only_transformer_gb300 import binding, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ERR = 2e-2
+MEAN_ERR = 2e-3
+LN2 = math.log(2.0)
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    h = binding.Attention(0)
+    yield h
+    assert h.get_error() == 0
+    h.close()
+
+
+def _gpu(attn, wl, kind):
+    out = attn.forward(wl.qkv.cuda(), wl.cu_seqlens.cuda(), kind)
+    torch.cuda.synchronize()
+    assert attn.get_error() == 0
+    return out.cpu().double().numpy()
+
+
+# How far the kernels' fp32 rotated value may sit from the exact one, per
+# unit of |x_m| + |x_m+32| (the pair's magnitudes), with a margin of about 3:
+# global layers rotate with an fp32 table of fp64 cos/sin (table error
+# <= 2^-25, two fp32 roundings: <= 2^-22.7 in all); local layers compute
+# cos/sin in the kernel (fast sine and cosine <= 2^-21.2 on [-pi, pi], the
+# angle's fp32 rounding, one angle addition for positions 128 back: about
+# 1.3e-6 = 2^-19.6).
+ROT_EPS = {"global": 2.0 ** -21, "local": 2.0 ** -18}
+
+
+def _rotated(x, theta):
+    """Exact rotated rows (fp64) of x[L, 64] at positions 0 .. L-1."""
+    return oracle.rope_rows(x, np.arange(x.shape[0]), theta)
+
+
+def _scores_head0(wl, s, kind):
+    """Scores q~.k~ / 8 of head 0 of sequence s on the rounded rotated rows
+    (oracle RoPE, oracle rounding), fp64 [L, L]."""
+    theta = oracle.KINDS[kind]["theta"]
+    b, e = int(wl.cu_seqlens[s]), int(wl.cu_seqlens[s + 1])
+    x = wl.qkv[b:e].double().numpy()
+    q = oracle.round_bf16(_rotated(x[:, 0:64], theta))
+    k = oracle.round_bf16(_rotated(x[:, 768:832], theta))
+    return q @ k.T / 8.0
+
+
+def _flip_step(x, eps_rel, theta):
+    """Rounded rotated rows and, per element, the distance between the two
+    bf16 values an fp32 rotation within eps of the exact one may round to
+    (0 where both round the same)."""
+    y = _rotated(x, theta)
+    mag = np.abs(x[:, :32]) + np.abs(x[:, 32:])
+    eps = eps_rel * np.concatenate([mag, mag], axis=1)
+    return oracle.round_bf16(y), oracle.round_bf16(y + eps) - oracle.round_bf16(y - eps)
+
+
+def _tolerance_terms(wl, kind):
+    """Per output element, the two derived terms of the module docstring:
+    (operand-rounding term without its factor 2, bf16 rounding term), each
+    fp64 [T, 768]."""
+    p = oracle.KINDS[kind]
+    theta, hw = p["theta"], p["half_window"]
+    flip = np.zeros((wl.T, 768))
+    bf16 = np.zeros((wl.T, 768))
+    cu = wl.cu_seqlens.tolist()
+    for s in range(len(cu) - 1):
+        b, e = cu[s], cu[s + 1]
+        L = e - b
+        if L == 0:
+            continue
+        x = wl.qkv[b:e].double().numpy()
+        i = np.arange(L)
+        keep = np.ones((L, L), dtype=bool) if hw < 0 else np.abs(i[:, None] - i[None, :]) <= hw
+        for h in range(12):
+            q, uq = _flip_step(x[:, 64 * h:64 * h + 64], ROT_EPS[kind], theta)
+            k, uk = _flip_step(x[:, 768 + 64 * h:768 + 64 * h + 64], ROT_EPS[kind], theta)
+            v = x[:, 1536 + 64 * h:1536 + 64 * h + 64]
+            sc = np.where(keep, q @ k.T / 8.0, -np.inf)
+            w = np.exp(sc - sc.max(axis=1, keepdims=True))
+            w /= w.sum(axis=1, keepdims=True)
+            o = w @ v
+            a = w * np.expm1((uq @ np.abs(k).T + np.abs(q) @ uk.T) / 8.0)
+            cols = slice(64 * h, 64 * h + 64)
+            flip[b:e, cols] = a @ np.abs(v) + a.sum(axis=1, keepdims=True) * np.abs(o)
+            bf16[b:e, cols] = 2.0 ** -8 * (w @ np.abs(v) + np.abs(o))
+    return flip, bf16
+
+
+def _local_rescale_rows(sc):
+    """Rows whose softmax meets a key, outside the 32-key chunk that holds the
+    row's own position (the chunk the local kernel takes its first reference
+    maximum from), more than 64 binary orders of magnitude above that chunk's
+    maximum: the local kernel must raise its reference and rescale."""
+    L = sc.shape[0]
+    hits = 0
+    for i in range(L):
+        lo, hi = max(0, i - 64), min(L - 1, i + 64)
+        c0 = 32 * (i // 32)
+        ref = sc[i, c0:min(c0 + 32, hi + 1)].max()
+        others = np.concatenate([sc[i, lo:c0], sc[i, c0 + 32:hi + 1]])
+        if others.size and (others.max() - ref) / LN2 > 64.0:
+            hits += 1
+    return hits
+
+
+def _global_rescale_rows(sc):
+    """Rows with a 128-key tile whose maximum exceeds the maximum of every
+    earlier tile by more than 8 binary orders of magnitude: the global kernel
+    must move its reference (inside a segment) or merge states of very
+    different maxima (across a split)."""
+    L = sc.shape[0]
+    nt = (L + 127) // 128
+    tmax = np.stack([sc[:, 128 * t:min(L, 128 * t + 128)].max(axis=1) for t in range(nt)], axis=1)
+    run = np.maximum.accumulate(tmax, axis=1)
+    jump = (tmax[:, 1:] - run[:, :-1]) / LN2
+    return int((jump > 8.0).any(axis=1).sum()) if nt > 1 else 0
+
+
+def _check_against_rounded(attn, wl, kind):
+    got = _gpu(attn, wl, kind)
+    ref, _ = oracle.attention_kind(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), kind,
+                                   round_operands=True)
+    what = f"{wl.name} {kind} (rounded operands)"
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    flip, bf16 = _tolerance_terms(wl, kind)
+    widened = float((2.0 * flip > MAX_ERR).mean())
+    extra = 2.0 * flip + bf16
+    over = err > MAX_ERR + extra
+    assert not over.any(), \
+        f"{what}: {int(over.sum())} elements beyond the tolerance (max|err| {err.max():.3e}, " \
+        f"worst excess {(err - MAX_ERR - extra).max():.3e})"
+    assert err.mean() <= MEAN_ERR, f"{what}: mean|err| {err.mean():.3e}"
+    # the local kernel's in-kernel angles make its eps 8x the global one, and
+    # at sigma 8 about a quarter of its elements get a wider tolerance
+    assert widened < 0.3, f"{what}: the operand-rounding term widens {widened:.1%} of the elements"
+    return got
+
+
+# ---------------------------------------------------------------------------
+# Q and K with a wide spread
+# ---------------------------------------------------------------------------
+
+WIDE_PACKS = {"eight_seqs": [463, 199, 96, 332, 511, 64, 270, 130], "seq1000": [1000]}
+
+
+@pytest.mark.parametrize("sigma", [4.0, 8.0])
+@pytest.mark.parametrize("pack", list(WIDE_PACKS))
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_wide_score_range(attn, kind, pack, sigma):
+    wl = W.custom(WIDE_PACKS[pack], seed=300 + int(sigma), sigma_qk=sigma)
+    if sigma == 8.0 or kind == "global":
+        s = int(np.argmax(wl.lengths))
+        sc = _scores_head0(wl, s, kind)
+        reached = _local_rescale_rows(sc) if kind == "local" else _global_rescale_rows(sc)
+        assert reached > 0, "input does not reach the rescaling path"
+    _check_against_rounded(attn, wl, kind)
+
+
+# ---------------------------------------------------------------------------
+# keys that tower over the rest
+# ---------------------------------------------------------------------------
+
+SPIKE_PACKS = {
+    # one sequence of 3000: 24 key tiles per query block, while each of the
+    # 152 CTAs gets about 22.7 (block, head, tile) iterations of the global
+    # split, so every global query block is cut between CTAs and merged
+    "seq3000": [3000],
+    "mixed": [1000, 300, 77, 1, 129],
+    "ragged": [1000, 3, 777],
+}
+
+
+@pytest.mark.parametrize("pack", list(SPIKE_PACKS))
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_spiked_keys(attn, kind, pack):
+    wl = W.spiked(SPIKE_PACKS[pack], seed=700 + len(pack), every=37, factor=32.0)
+    s = int(np.argmax(wl.lengths))
+    sc = _scores_head0(wl, s, kind)
+    reached = _local_rescale_rows(sc) if kind == "local" else _global_rescale_rows(sc)
+    assert reached > 0, "input does not reach the rescaling path"
+    if kind == "global" and pack == "seq3000":
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        L = wl.lengths[0]
+        tiles = (L + 127) // 128
+        total = ((L + 255) // 256) * 12 * tiles
+        assert total / min(sms, total) < tiles, "no query block is split between CTAs"
+    _check_against_rounded(attn, wl, kind)
+
+
+# ---------------------------------------------------------------------------
+# the band's edges, on the attention kernels' own masks
+# ---------------------------------------------------------------------------
+
+PROBE_PACKS = {
+    "len1": [1],
+    "tile_edges": [127, 128, 129],
+    "window_edges": [64, 65, 66, 193, 194],
+    "empties": [0, 5, 0, 300, 0],
+    "long_ragged": [1000, 3, 777],
+    "seq8192": [8192],
+}
+
+
+def _check_probe(got, ref, what):
+    err = np.abs(got - ref)
+    bound = 2.0 ** -8 * np.abs(ref) * 1.001
+    bad = err > bound
+    assert not bad.any(), \
+        f"{what}: {int(bad.sum())} elements off by more than one bf16 rounding " \
+        f"(worst {err.max():.3e} at {np.unravel_index(np.argmax(err - bound), err.shape)})"
+
+
+@pytest.mark.parametrize("pack", list(PROBE_PACKS))
+@pytest.mark.parametrize("kind", ["global", "local"])
+def test_band_probe(attn, kind, pack):
+    wl = W.band_probe(PROBE_PACKS[pack])
+    got = _gpu(attn, wl, kind)
+    rows = None
+    if kind == "global" and wl.T > 4000:
+        # every row of the first and last three tiles, and a seeded sample
+        rows = np.unique(np.concatenate([np.arange(384), np.arange(wl.T - 384, wl.T),
+                                         W.sample_rows(wl.cu_seqlens, 256, seed=5)]))
+        got = got[rows]
+    ref, _ = oracle.attention_kind(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), kind, rows=rows)
+    _check_probe(got, ref, f"{wl.name} {kind}")
+    # the probe reads the admitted-set size back from the outputs: every
+    # head's 64 columns of row i sum to 16 |A_i| / |A_i| = 16 exactly
+    if got.size:
+        np.testing.assert_allclose(got.reshape(-1, 12, 64).sum(axis=2), 16.0, rtol=2e-2)
+
+
+def test_band_probe_many_tiny_sequences(attn):
+    g = torch.Generator().manual_seed(79)
+    lengths = torch.randint(1, 21, (300,), generator=g).tolist()
+    wl = W.band_probe(lengths)
+    for kind in ("global", "local"):
+        got = _gpu(attn, wl, kind)
+        ref, _ = oracle.attention_kind(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(), kind)
+        _check_probe(got, ref, f"{wl.name} {kind}")
+
+
+def test_band_probe_wide_band():
+    """A half window of 100 (beyond the two-tile band kernel's reach) runs
+    the generic kernel; its band edges are probed the same way."""
+    h = binding.Attention(0, half_window=100)
+    try:
+        wl = W.band_probe([250, 64, 300])
+        got = h.forward(wl.qkv.cuda(), wl.cu_seqlens.cuda(), "local").cpu().double().numpy()
+        assert h.get_error() == 0
+        ref, _ = oracle.attention(W.bf16_bits(wl.qkv), wl.cu_seqlens.numpy(),
+                                  oracle.KINDS["local"]["theta"], 100)
+        _check_probe(got, ref, "half window 100")
+    finally:
+        h.close()
