@@ -45,9 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 N_SETS = 6
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# the ncu captures of the one-sequence 8192-token workload summarised in
-# profiles/*_kernel_config3.md.  Reported only while the
-# kernel sources still hash to what was captured.
+# one ncu capture of each kernel on the one-sequence 8192-token workload.
+# Reported only while the kernel sources still hash to what was captured.
 NCU_TRAFFIC = {
     "global": {"bytes": 39.58e6, "kernel": "attn_global_kernel",
                "sources": {"attn_global.cu": "e38807e445b93991", "common.cuh": "c9dc0987f95761ca"}},
@@ -123,6 +122,15 @@ def captured_traffic(kind, workload):
         except OSError:
             return None
     return rec["bytes"]
+
+
+def bench_config(workload, desc, wl, world):
+    """The `config` object of both arms' JSON lines (the same workload)."""
+    return {"workload": f"{workload}: {desc}; step = 1 global + 1 local layer",
+            "tokens_per_step_per_gpu": wl.T, "n_seqs": wl.n_seqs,
+            "l2": f"inputs larger than L2 across steps: {N_SETS} rotating qkv/out buffer sets "
+                  "on the GPU (the oracle arm reads host memory)",
+            "parallelism": f"{world} independent replica(s), no collective"}
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -697,6 +705,8 @@ def run_ours(args):
                     "event pair around each attention kernel; roofline_frac of the schedule = the "
                     "sum of the layers' roofline times over the measured time"}
     g, lo = layers["global"], layers["local"]
+    calls = {"global": "plan_kernel, rope_qk_kernel, attn_global_kernel",
+             "local": "attn_local_kernel" if wl.n_seqs <= 256 else "plan_kernel, attn_local_kernel"}
     # The dominant kernel (the global layer's) against the tensor peak; the
     # local layer's kernel, HBM bound, against the copy bandwidth.  Kernel
     # times are CUDA-event pairs around each launch over a second pass of
@@ -705,13 +715,19 @@ def run_ours(args):
     # peaks.
     roofline = {"bound": "tensor", "achieved": g["tflops"], "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": g["tflops"] / peaks["bf16_tflops"],
+                "frac_call": g["roofline_frac_call"],
                 "traffic": captured_traffic("global", args.workload),
                 "kernel": "attn_global_kernel (global layer)",
+                "call": f"frac_call: the whole global call ({calls['global']}), from one event "
+                        f"pair around {kk} back-to-back calls enqueued ahead of the GPU",
                 "peak_source": f"{src} bf16_tflops (burst)"}
     roofline_local = {"bound": "hbm", "achieved": lo["hbm_gbs"], "peak": peaks["hbm_gbs"],
                       "unit": "GB/s", "frac": lo["hbm_gbs"] / peaks["hbm_gbs"],
+                      "frac_call": lo["roofline_frac_call"],
                       "traffic": captured_traffic("local", args.workload),
                       "kernel": "attn_local_kernel (local layer)",
+                      "call": f"frac_call: the whole local call ({calls['local']}), from one event "
+                              f"pair around {kk} back-to-back calls enqueued ahead of the GPU",
                       "peak_source": f"{src} hbm_gbs"}
     rec = {
         "metric": METRIC,
@@ -726,12 +742,9 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {desc}; step = 1 global + 1 local layer",
-                   "tokens_per_step_per_gpu": T, "n_seqs": wl.n_seqs,
-                   "l2": f"{N_SETS} rotating input/output buffer sets (inputs > L2 across steps)",
-                   "timing": "value: one CUDA event pair around K steps; kernel durations: an event "
-                             "pair around each attention kernel over a second pass of the K steps",
-                   "parallelism": f"{world} independent replica(s), no collective"},
+        "config": bench_config(args.workload, desc, wl, world),
+        "timing": "value: one CUDA event pair around K steps; kernel durations: an event "
+                  "pair around each attention kernel over a second pass of the K steps",
         "layers": layers,
         "out_proj": out_proj,
         "ln_qkv": ln_qkv,
@@ -771,23 +784,29 @@ def run_reference(args):
     nl = int(min(wl.T, max(2, per_step / 2 / max(probe["local"][0], 1e-9))))
     for i in range(args.warmup):
         time_oracle(wl, ng, nl, seed=100 + i)
-    secs = 0.0
+    per_token = 0.0
     rows = None
+    t0 = time.perf_counter()
     for i in range(args.steps):
         r, cores = time_oracle(wl, ng, nl, seed=1000 + i)
-        secs += r["global"][0] + r["local"][0]
+        per_token += r["global"][0] + r["local"][0]
         rows = (r["global"][1], r["local"][1])
-    sec_per_token = secs / args.steps
+    wall_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    sec_per_token = per_token / args.steps
     value = 1.0 / sec_per_token
     sample = (f"fp64 oracle, per step {rows[0]} sampled query rows of the global layer and "
-              f"{rows[1]} of the local layer (all 12 heads), extrapolated to {wl.T} tokens")
+              f"{rows[1]} of the local layer (all 12 heads); tokens/s = 1 / (seconds per "
+              "row of the global layer + seconds per row of the local layer)")
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * sec_per_token * wl.T,
+        "warmup": args.warmup, "ms_per_step": wall_ms,
+        "ms_per_step_extrapolated": 1e3 * sec_per_token * wl.T,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": f"{args.workload}: {desc}; step = 1 global + 1 local layer",
-                   "tokens_per_step_per_gpu": wl.T},
+        "config": bench_config(args.workload, desc, wl, world),
+        "timing": "ms_per_step: wall time of each timed step, a bounded sample of the "
+                  "workload's query rows; ms_per_step_extrapolated: the same rate over every "
+                  f"row of the {wl.T}-token step",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
