@@ -140,11 +140,11 @@ struct AttnArgs {
 constexpr int kPartialRows = 256;
 constexpr int kPartialFloats = kPartialRows * 64 + kPartialRows * 2;
 
-// RoPE constants for computing cos/sin in the kernel: for pair m the
+// RoPE constants for computing cos/sin in the local kernel: for pair m the
 // frequency in turns per position as a 64-bit binary fraction (frac_hi holds
 // 2^-1 .. 2^-32, frac_lo 2^-33 .. 2^-64), so that the turns of any position
 // are exact modulo 1 in integer arithmetic, and the rotation by 128
-// positions.
+// positions (cos, sin of 128 w, fp64 values rounded to fp32).
 struct RopeConsts {
     uint32_t frac_hi[kPairsConst];
     uint32_t frac_lo[kPairsConst];
