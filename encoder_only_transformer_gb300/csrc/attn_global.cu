@@ -361,21 +361,33 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
             const float neg = -mn;
 
             // p = 2^(s * scale - m), packed to bf16 pairs; row sum in 4
-            // independent fp32x2 accumulators
+            // independent packed fp32x2 accumulators
             uint32_t pk[kBlockN / 2];
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // one asm block per score pair: the exponent on the packed
+            // fp32x2 path, the two exponentials, the pair added to one of four
+            // packed row-sum accumulators, and the bf16 pack of P
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            const uint64_t sc2 = f2(kScaleLog2, kScaleLog2), nm2 = f2(neg, neg);
 #pragma unroll
             for (int i = 0; i < kBlockN / 2; ++i) {
-                float x0 = sc[2 * i], x1 = sc[2 * i + 1];
-                ffma2_bc(x0, x1, kScaleLog2, neg);
-                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                const int a = 2 * (i & 3);
-                fadd2(acc[a], acc[a + 1], p0, p1);
-                pk[i] = pack_bf16x2(p0, p1);
+                asm("{\n\t.reg .b64 y, pp;\n\t.reg .f32 y0, y1, p0, p1;\n\t"
+                    "mov.b64 y, {%2, %3};\n\t"
+                    "fma.rn.f32x2 y, y, %4, %5;\n\t"
+                    "mov.b64 {y0, y1}, y;\n\t"
+                    "ex2.approx.ftz.f32 p0, y0;\n\t"
+                    "ex2.approx.ftz.f32 p1, y1;\n\t"
+                    "mov.b64 pp, {p0, p1};\n\t"
+                    "add.f32x2 %1, %1, pp;\n\t"
+                    "cvt.rn.bf16x2.f32 %0, p1, p0;\n\t}"
+                    : "=r"(pk[i]), "+l"(acc2[i & 3])
+                    : "f"(sc[2 * i]), "f"(sc[2 * i + 1]), "l"(sc2), "l"(nm2));
             }
-            fadd2(acc[0], acc[1], acc[2], acc[3]);
-            fadd2(acc[4], acc[5], acc[6], acc[7]);
-            fadd2(acc[0], acc[1], acc[4], acc[5]);
+            uint64_t accs = acc2[0];
+            asm("add.f32x2 %0, %0, %1;" : "+l"(accs) : "l"(acc2[1]));
+            asm("add.f32x2 %0, %0, %1;" : "+l"(accs) : "l"(acc2[2]));
+            asm("add.f32x2 %0, %0, %1;" : "+l"(accs) : "l"(acc2[3]));
+            float acc0, acc1;
+            f2_split(accs, acc0, acc1);
 
             if (t > 0) {
                 // P_w and O_w are free once the previous P V has completed
@@ -396,7 +408,7 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
                     }
                 }
             }
-            l = l * alpha + (acc[0] + acc[1]);
+            l = l * alpha + (acc0 + acc1);
             m = mn;
             tmem_st64(tP, pk);
             tmem_wait_st();
