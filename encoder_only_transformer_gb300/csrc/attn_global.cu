@@ -342,13 +342,14 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
                     if (i >= kvalid)
                         sc[i] = -INFINITY;
             }
-            // row maximum: 8 independent chains of 3-input max, then combine
+            // row maximum: 8 independent chains (columns 0-15 by 2-input
+            // max, then 16 columns per step by 3-input max), then combine
             float mp[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                mp[k] = fmax3(sc[k], sc[8 + k], sc[16 + k]);
+                mp[k] = fmaxf(sc[k], sc[8 + k]);
 #pragma unroll
-            for (int i = 24; i < kBlockN; i += 16)
+            for (int i = 16; i < kBlockN; i += 16)
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mp[k] = fmax3(mp[k], sc[i + k], sc[i + 8 + k]);
