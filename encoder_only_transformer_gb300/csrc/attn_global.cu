@@ -42,8 +42,8 @@ namespace mbert {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kRegsSoftmax = 208;   // 4 x 88 + 8 x 208 = 12 x 168 (the launch budget)
-constexpr int kRegsControl = 88;
+constexpr int kRegsSoftmax = 216;   // 4 x 72 + 8 x 216 = 12 x 168 (the launch budget)
+constexpr int kRegsControl = 72;
 constexpr int kStages = 3;
 
 constexpr uint32_t kOffQ = 0;                                  // 2 sets of (Q0, Q1)
