@@ -470,14 +470,22 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
             if (write) {
                 // Merge every segment's state (this CTA's included) in CTA
                 // order, so that the result does not depend on which CTA
-                // finished last.
+                // finished last.  When this CTA holds the first segment (the
+                // usual case: its last segment is the unit's first), its own
+                // state is already the running state; the first merge step
+                // would reproduce it exactly (weights 0 and 1).
                 const int c_first = cta_of(p, ua), c_last = cta_of(p, ub - 1);
-                m = -INFINITY;
-                l = 0.f;
+                int cc = c_first;
+                if (c_first == cta) {
+                    ++cc;
+                } else {
+                    m = -INFINITY;
+                    l = 0.f;
 #pragma unroll
-                for (int i = 0; i < kHeadDim; ++i)
-                    o[i] = 0.f;
-                for (int cc = c_first; cc <= c_last; ++cc) {
+                    for (int i = 0; i < kHeadDim; ++i)
+                        o[i] = 0.f;
+                }
+                for (; cc <= c_last; ++cc) {
                     const float *part = partial_slot(p, slot_of(p, cc, ua));
                     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(part + kPartialRows * kHeadDim) + rr);
                     const float mnew = fmaxf(m, ml.x);
