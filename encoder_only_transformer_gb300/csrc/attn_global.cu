@@ -126,7 +126,16 @@ struct SegIter {
     {
         it = range_lo(p, c);
         hi = range_lo(p, c + 1);
-        int lo = 0, h = p.entries;           // entry with tile_start <= it
+        // the entry with tile_start <= it < its successor's: first a guess
+        // as if all entries had the same iterations (exact for one sequence,
+        // two independent loads), then a binary search on the side it missed
+        const int e = min(static_cast<int>((it * p.entries) / p.total), p.entries - 1);
+        const long long t0 = p.tile_start[e], t1 = p.tile_start[e + 1];
+        if (t0 <= it && it < t1) {
+            entry = e;
+            return;
+        }
+        int lo = it < t0 ? 0 : e + 1, h = it < t0 ? e : p.entries;
         while (h - lo > 1) {
             const int mid = (lo + h) >> 1;
             if (p.tile_start[mid] <= it)
