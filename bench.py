@@ -706,7 +706,7 @@ def run_ours(args):
                     "event pair around each attention kernel; roofline_frac of the schedule = the "
                     "sum of the layers' roofline times over the measured time"}
     g, lo = layers["global"], layers["local"]
-    calls = {"global": "plan_kernel, rope_qk_kernel, attn_global_kernel",
+    calls = {"global": "plan_rope_kernel, attn_global_kernel",
              "local": "attn_local_kernel" if wl.n_seqs <= 256 else "plan_kernel, attn_local_kernel"}
     # The dominant kernel (the global layer's) against the tensor peak; the
     # local layer's kernel, HBM bound, against the copy bandwidth.  Kernel

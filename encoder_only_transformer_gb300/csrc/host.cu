@@ -540,17 +540,15 @@ int forward_impl(mbert_attn *h, const void *qkv, const int32_t *cu_seqlens, int 
         h->last_stream = st;
         return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
     }
-    e = launch_plan(p, st);
-    if (e == cudaSuccess)
-        e = launch_rope_qk(p, static_cast<const __nv_bfloat16 *>(qkv), h->rope[layer_kind],
-                           h->cfg.max_seqlen, h->rot, st);
+    e = launch_plan_rope(p, static_cast<const __nv_bfloat16 *>(qkv), h->rope[layer_kind],
+                         h->cfg.max_seqlen, h->rot, st);
     if (e == cudaSuccess && ev0)
         e = cudaEventRecord(ev0, st);
     if (e == cudaSuccess)
         e = layer_kind == MBERT_GLOBAL ? launch_attn_global(a, st) : launch_attn_generic(a, st);
     if (e == cudaSuccess && ev1)
         e = cudaEventRecord(ev1, st);
-    h->launches += 3;
+    h->launches += 2;
     h->last_stream = st;
     return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
 }

@@ -109,9 +109,10 @@ struct Plan {
 
 cudaError_t launch_plan(const Plan &p, cudaStream_t stream);
 
-// Rotate Q and K of every row (all heads) into rot[T][1536] bf16.
-cudaError_t launch_rope_qk(const Plan &p, const __nv_bfloat16 *qkv, const float2 *table,
-                           int table_rows, __nv_bfloat16 *rot, cudaStream_t stream);
+// The plan and, in the same launch, the RoPE of Q and K of every row (all
+// heads) into rot[T][1536] bf16.
+cudaError_t launch_plan_rope(const Plan &p, const __nv_bfloat16 *qkv, const float2 *table,
+                             int table_rows, __nv_bfloat16 *rot, cudaStream_t stream);
 
 // Admitted-key count per query row, from the attention kernels' tile
 // schedule and mask.

@@ -45,12 +45,11 @@ __device__ int block_inclusive_scan(int v, int *warp_sums)
 // its ceil(L/blk) query blocks of blk rows, sequences ordered by decreasing block count
 // (longest-processing-time first; the order inside a bin is arbitrary and
 // does not affect any result).
-__global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seqlen, int blk,
-            int cu_short_ok, int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count,
-            int32_t *__restrict__ tile_start, int32_t *__restrict__ unit_cnt)
+__device__ void plan_block(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seqlen, int blk,
+                           int cu_short_ok, int32_t *err, int2 *__restrict__ work,
+                           int32_t *__restrict__ work_count, int32_t *__restrict__ tile_start,
+                           int32_t *__restrict__ unit_cnt)
 {
-    pdl_wait();
     __shared__ int s_bad;
     __shared__ int s_hist[kMaxBins + 1];
     __shared__ int s_off[kMaxBins + 1];
@@ -138,6 +137,15 @@ plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seq
         tile_start[total] = s_carry;
     for (int i = tid; i < total * kHeads; i += kPlanThreads)
         unit_cnt[i] = 0;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seqlen, int blk,
+            int cu_short_ok, int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count,
+            int32_t *__restrict__ tile_start, int32_t *__restrict__ unit_cnt)
+{
+    pdl_wait();
+    plan_block(cu, n_seqs, T, max_seqlen, blk, cu_short_ok, err, work, work_count, tile_start, unit_cnt);
     pdl_trigger();
 }
 
@@ -155,24 +163,24 @@ __device__ __forceinline__ int seq_of_row(const int32_t *__restrict__ cu, int n_
     return lo;
 }
 
-constexpr int kRopeRowsPerCta = 4;
 constexpr int kRopeThreadsPerRow = 2 * kHeads * (kPairs / 8);   // 96: 24 head blocks x 4 chunks
+constexpr int kRopeRowsPerCta = kPlanThreads / kRopeThreadsPerRow;   // 10 rows of a 1024-thread block
 
 // Rotate-half RoPE of Q and K ("ModernBERT" (candding), "The two rope
 // tables"): for pair m = (x[m], x[m+32]) at position p,
 //   y[m] = x[m] cos - x[m+32] sin,  y[m+32] = x[m+32] cos + x[m] sin,
 // with (cos, sin) of p * base^(-2m/64) from the fp32 table.  Each thread
-// rotates 8 pairs of one head of Q or K; the result is rounded to bf16.
-__global__ void __launch_bounds__(kRopeRowsPerCta * kRopeThreadsPerRow)
-rope_qk_kernel(const __nv_bfloat16 *__restrict__ qkv, const int32_t *__restrict__ cu, int n_seqs,
-               long long T, const float2 *__restrict__ table, int table_rows,
-               const int32_t *__restrict__ work_count, __nv_bfloat16 *__restrict__ rot)
+// rotates 8 pairs of one head of Q or K, rows 10 b .. 10 b + 9 for block b;
+// the result is rounded to bf16.  Positions come from cu_seqlens by binary
+// search; with cu_seqlens the plan rejects, the rows still land in rot[T]
+// (and the table index is clamped), and the attention kernel reads none.
+__device__ void rope_block(long long b, const __nv_bfloat16 *__restrict__ qkv,
+                           const int32_t *__restrict__ cu, int n_seqs, long long T,
+                           const float2 *__restrict__ table, int table_rows, __nv_bfloat16 *__restrict__ rot)
 {
-    pdl_wait();
-    if (*work_count <= 0)
-        return;   // the plan's checks failed: positions are unknown
-    const long long row = static_cast<long long>(blockIdx.x) * kRopeRowsPerCta
-                          + threadIdx.x / kRopeThreadsPerRow;
+    if (threadIdx.x >= kRopeRowsPerCta * kRopeThreadsPerRow)
+        return;
+    const long long row = b * kRopeRowsPerCta + threadIdx.x / kRopeThreadsPerRow;
     if (row >= T)
         return;
     const int sub = threadIdx.x % kRopeThreadsPerRow;
@@ -184,10 +192,10 @@ rope_qk_kernel(const __nv_bfloat16 *__restrict__ qkv, const int32_t *__restrict_
     const int col = blk * kHeadDim + chunk * 8;
 
     const uint4 a = __ldg(reinterpret_cast<const uint4 *>(qkv + row * kQKVWidth + col));
-    const uint4 b = __ldg(reinterpret_cast<const uint4 *>(qkv + row * kQKVWidth + col + kPairs));
+    const uint4 bb = __ldg(reinterpret_cast<const uint4 *>(qkv + row * kQKVWidth + col + kPairs));
     const float4 *cs = reinterpret_cast<const float4 *>(table + static_cast<long long>(pos) * kPairs + chunk * 8);
     const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+    const uint32_t bv[4] = {bb.x, bb.y, bb.z, bb.w};
     uint32_t ya[4], yb[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -204,6 +212,22 @@ rope_qk_kernel(const __nv_bfloat16 *__restrict__ qkv, const int32_t *__restrict_
     constexpr int kRotWidth = 2 * kHidden;
     *reinterpret_cast<uint4 *>(rot + row * kRotWidth + col) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
     *reinterpret_cast<uint4 *>(rot + row * kRotWidth + col + kPairs) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+}
+
+// The plan and the RoPE pass in one launch: block 0 builds the plan, blocks
+// 1.. rotate rows.  The RoPE pass does not read the plan.
+__global__ void __launch_bounds__(kPlanThreads)
+plan_rope_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int max_seqlen, int blk,
+                 int cu_short_ok, int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count,
+                 int32_t *__restrict__ tile_start, int32_t *__restrict__ unit_cnt,
+                 const __nv_bfloat16 *__restrict__ qkv, const float2 *__restrict__ table, int table_rows,
+                 __nv_bfloat16 *__restrict__ rot)
+{
+    pdl_wait();
+    if (blockIdx.x == 0)
+        plan_block(cu, n_seqs, T, max_seqlen, blk, cu_short_ok, err, work, work_count, tile_start, unit_cnt);
+    else
+        rope_block(blockIdx.x - 1, qkv, cu, n_seqs, T, table, table_rows, rot);
     pdl_trigger();
 }
 
@@ -287,13 +311,13 @@ cudaError_t launch_plan(const Plan &p, cudaStream_t stream)
                           p.work_count, p.tile_start, p.unit_cnt);
 }
 
-cudaError_t launch_rope_qk(const Plan &p, const __nv_bfloat16 *qkv, const float2 *table,
-                           int table_rows, __nv_bfloat16 *rot, cudaStream_t stream)
+cudaError_t launch_plan_rope(const Plan &p, const __nv_bfloat16 *qkv, const float2 *table,
+                             int table_rows, __nv_bfloat16 *rot, cudaStream_t stream)
 {
-    const long long blocks = (p.T + kRopeRowsPerCta - 1) / kRopeRowsPerCta;
-    return launch_chained(rope_qk_kernel, dim3(static_cast<unsigned>(blocks)),
-                          dim3(kRopeRowsPerCta * kRopeThreadsPerRow), 0, stream, qkv, p.cu, p.n_seqs,
-                          p.T, table, table_rows, p.work_count, rot);
+    const long long blocks = 1 + (p.T + kRopeRowsPerCta - 1) / kRopeRowsPerCta;
+    return launch_chained(plan_rope_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kPlanThreads), 0, stream,
+                          p.cu, p.n_seqs, p.T, p.max_seqlen, p.block, p.cu_short_ok ? 1 : 0, p.err, p.work,
+                          p.work_count, p.tile_start, p.unit_cnt, qkv, table, table_rows, rot);
 }
 
 cudaError_t launch_key_count(const Plan &p, int half_window, int32_t *counts, cudaStream_t stream)
