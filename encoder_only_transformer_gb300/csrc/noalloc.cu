@@ -10,8 +10,8 @@
 // rotated Q/K rows and the two RoPE tables) from one file-scope static
 // __device__ array.
 //
-// It is not the benchmarked path: for both layer kinds it runs the plan
-// kernel, the RoPE pass into the static rotated-Q/K rows and the generic
+// It is not the benchmarked path: for both layer kinds it runs the plan and
+// the RoPE pass into the static rotated-Q/K rows (one launch), then the generic
 // attention kernel (one CTA per 128-query block and head), not the
 // persistent global and local kernels of mbert_attn_forward.  Its results
 // agree with the oracle within the same bounds; its speed and its fp32

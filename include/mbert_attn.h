@@ -257,7 +257,7 @@ int mbert_attn_selftest_timeout(mbert_attn *h, int64_t limit_us, void *stream);
  * there, so two calls whose work overlaps on the GPU (e.g. on different
  * streams) race.
  * This is not the benchmarked path: for both layer kinds it runs the plan
- * kernel, a RoPE pass into the static rotated-Q/K rows and the generic
+ * and a RoPE pass into the static rotated-Q/K rows (one launch), then the generic
  * attention kernel (one CTA per 128-query block and head), not the
  * persistent kernels of mbert_attn_forward, so its speed and its fp32
  * summation order differ; its results meet the same bounds against the
