@@ -66,9 +66,11 @@ constexpr int kBarODone = 22;
 constexpr int kBarOFree = 24;
 constexpr int kBarSegSync = 26;   // all 256 softmax threads wrote their partial rows
 constexpr int kBarSegFlag = 27;   // the counter result is in shared memory
-constexpr int kNumBars = 28;
+constexpr int kBarEarly = 28;     // the early look at the last segment's unit is in shared memory
+constexpr int kNumBars = 29;
 constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;          // TMEM address
 constexpr uint32_t kOffFlag = kOffSlot + 8;                    // "I merge" flag
+constexpr uint32_t kOffEarly = kOffFlag + 4;                   // early-look result
 
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int w) { return 128u * w; }
@@ -317,6 +319,18 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
     uint32_t g0 = 0, npartial = 0;
     for (uint32_t sg = 0; si.next(p, s); ++sg) {
         const int n = s.ke - s.kb;
+        // The CTA's last segment, when it is the first of a unit cut between
+        // CTAs (the usual case at the end of a range): the unit's other
+        // segments ran at the start of the next CTAs' ranges.  One thread
+        // reads the unit's counter now (acquire), while the segment runs; if
+        // they are all in, this segment merges at its end without leaving
+        // its own state in the workspace.
+        const bool early = si.it >= si.hi && s.kb == 0 && n != s.ntiles;
+        const bool looker = early && w == 0 && r == 0;
+        int early_done = -1;
+        if (looker)
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
+                         : "=r"(early_done) : "l"(p.unit_cnt + s.entry * kHeads + s.head) : "memory");
         float m = -INFINITY;    // running reference maximum (scaled, base 2)
         float l = 0.f;          // running sum of exp2(score - m)
         for (int t = 0; t < n; ++t) {
@@ -448,33 +462,50 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
         mbar_arrive(bar(c, kBarOFree + w));   // the next segment may reset O
 
         bool write = true;
+        bool merge_now = false;
+        if (early) {
+            if (looker) {
+                *reinterpret_cast<volatile int *>(c.sbase + kOffEarly) =
+                    early_done == cta_of(p, s.ua + s.ntiles - 1) - cta;
+                mbar_arrive(bar(c, kBarEarly));
+            }
+            if (!mbar_wait(bar(c, kBarEarly), 0, p.err))
+                return;
+            merge_now = *reinterpret_cast<volatile int *>(c.sbase + kOffEarly) != 0;
+        }
         if (n != s.ntiles) {
             // The unit is split between CTAs: leave this segment's state in
-            // the workspace, and merge if this is the unit's last segment.
+            // the workspace, and merge if this is the unit's last segment
+            // (known from the early look, or from the unit's counter).
             const long long ua = s.ua, ub = s.ua + s.ntiles;
-            float *mine = partial_slot(p, slot_of(p, cta, ua));
-            float4 *dst = reinterpret_cast<float4 *>(mine + rr * kHeadDim);
+            if (!merge_now) {
+                float *mine = partial_slot(p, slot_of(p, cta, ua));
+                float4 *dst = reinterpret_cast<float4 *>(mine + rr * kHeadDim);
 #pragma unroll
-            for (int i = 0; i < kHeadDim / 4; ++i)
-                dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-            reinterpret_cast<float2 *>(mine + kPartialRows * kHeadDim)[rr] = make_float2(m, l);
-            __threadfence();
-            mbar_arrive(bar(c, kBarSegSync));
+                for (int i = 0; i < kHeadDim / 4; ++i)
+                    dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                reinterpret_cast<float2 *>(mine + kPartialRows * kHeadDim)[rr] = make_float2(m, l);
+                __threadfence();
+                mbar_arrive(bar(c, kBarSegSync));
+            }
             if (w == 0 && r == 0) {
-                int last = 0;
-                if (mbar_wait(bar(c, kBarSegSync), npartial & 1, p.err)) {
-                    const int c_first = cta_of(p, ua), c_last = cta_of(p, ub - 1);
-                    const int nseg = c_last - c_first + 1;
-                    const int unit = s.entry * kHeads + s.head;
-                    last = atomicAdd(p.unit_cnt + unit, 1) == nseg - 1;
-                    __threadfence();
+                int last = 1;
+                if (!merge_now) {
+                    last = 0;
+                    if (mbar_wait(bar(c, kBarSegSync), npartial & 1, p.err)) {
+                        const int c_first = cta_of(p, ua), c_last = cta_of(p, ub - 1);
+                        const int nseg = c_last - c_first + 1;
+                        const int unit = s.entry * kHeads + s.head;
+                        last = atomicAdd(p.unit_cnt + unit, 1) == nseg - 1;
+                        __threadfence();
+                    }
                 }
                 *flag = last;
                 mbar_arrive(bar(c, kBarSegFlag));
             }
             if (!mbar_wait(bar(c, kBarSegFlag), npartial & 1, p.err))
                 return;
-            ++npartial;
+            ++npartial;                                  // (SegSync is not used when merge_now: last segment)
             write = *flag != 0;
             if (write) {
                 // Merge every segment's state (this CTA's included) in CTA
@@ -591,6 +622,7 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
         }
         mbar_init(bar(c, kBarSegSync), 2 * kBlockM);
         mbar_init(bar(c, kBarSegFlag), 1);
+        mbar_init(bar(c, kBarEarly), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
