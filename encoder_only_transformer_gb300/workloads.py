@@ -86,6 +86,50 @@ def spiked(lengths, seed: int, every: int, factor: float) -> Workload:
                     x.to(torch.bfloat16), cu)
 
 
+def towering_keys(lengths, seed: int, heads: int = 6, first: float = 0.05,
+                  later: float = 40.0) -> Workload:
+    """N(0, 1) rows; in the first sequence and heads 0 .. heads-1 the K rows
+    of the first 128 keys are multiplied by `first` and every later K row by
+    `later`: scores that stay small over a query's first key tile and rise
+    hundreds of binary orders of magnitude above it afterwards."""
+    g = torch.Generator().manual_seed(seed)
+    lengths = [int(L) for L in lengths]
+    cu = cu_from_lengths(lengths)
+    x = torch.randn(int(cu[-1]), WIDTH, generator=g, dtype=torch.float32)
+    L0 = lengths[0] if lengths else 0
+    for h in range(heads):
+        cols = slice(OUT_WIDTH + 64 * h, OUT_WIDTH + 64 * h + 64)
+        x[0:min(128, L0), cols] *= first
+        x[128:L0, cols] *= later
+    return Workload(f"towering{lengths}", seed, 1.0, lengths, ["global"], x.to(torch.bfloat16), cu)
+
+
+def aligned_keys(lengths, seed: int, first: float = 0.2, later: float = 2.0,
+                 noise: float = 0.3) -> Workload:
+    """Per head one random direction u (norm 8): every Q row is u plus
+    N(0, noise^2) noise, every K row `first` (the first 128 keys of each
+    sequence) or `later` times u plus noise; V ~ N(0, 1).  A key near the
+    query's own position then scores close to |q| |k| / 8, so the scores of
+    later key tiles rise far above those of the first tile while staying
+    close to the Cauchy-Schwarz bound of the norms."""
+    g = torch.Generator().manual_seed(seed)
+    lengths = [int(L) for L in lengths]
+    cu = cu_from_lengths(lengths)
+    T = int(cu[-1])
+    x = torch.randn(T, WIDTH, generator=g, dtype=torch.float32)
+    for h in range(12):
+        u = torch.randn(64, generator=g)
+        u *= 8.0 / u.norm()
+        qc = slice(64 * h, 64 * h + 64)
+        kc = slice(OUT_WIDTH + 64 * h, OUT_WIDTH + 64 * h + 64)
+        x[:, qc] = u + noise * torch.randn(T, 64, generator=g)
+        scale = torch.full((T, 1), later)
+        for b in cu[:-1].tolist():
+            scale[b:b + 128] = first
+        x[:, kc] = scale * (u + noise * torch.randn(T, 64, generator=g))
+    return Workload(f"aligned{lengths}", seed, 1.0, lengths, ["global"], x.to(torch.bfloat16), cu)
+
+
 def band_probe(lengths, magnitude: float = 16.0) -> Workload:
     """Q = K = 0 and, in head h, V[t, h*64 + d] = magnitude when
     (t + h) % 64 == d, else 0 (t the packed row): no randomness.  Every key

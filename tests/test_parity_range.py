@@ -314,3 +314,71 @@ def test_band_probe_wide_band():
         _check_probe(got, ref, "half window 100")
     finally:
         h.close()
+
+
+# ---------------------------------------------------------------------------
+# scores that rise far above a query's first key tile
+# ---------------------------------------------------------------------------
+# The global kernel takes its reference from a segment's first key tile and
+# moves it (rescaling O and the row sum) only when a later tile's maximum
+# passes it by more than 8 binary orders of magnitude.  Two inputs make
+# that happen on nearly every row, each checked on the CPU first against a
+# unit's first tile, where every unit's first segment starts.
+
+
+def _first_tile_rise(wl):
+    """Per (sequence, head): each row's maximum score minus its maximum over
+    the first 128 keys, base 2, on the rounded rotated rows."""
+    theta = oracle.KINDS["global"]["theta"]
+    cu = wl.cu_seqlens.tolist()
+    out = {}
+    for s in range(len(cu) - 1):
+        b, e = cu[s], cu[s + 1]
+        x = wl.qkv[b:e].double().numpy()
+        for h in range(12):
+            q = oracle.round_bf16(_rotated(x[:, 64 * h:64 * h + 64], theta))
+            k = oracle.round_bf16(_rotated(x[:, 768 + 64 * h:768 + 64 * h + 64], theta))
+            sc = q @ k.T / 8.0 / LN2
+            out[s, h] = sc.max(axis=1) - sc[:, :128].max(axis=1)
+    return out
+
+
+def test_towering_keys(attn):
+    """Heads 0-5 of the first sequence: scores rise more than 128 binary
+    orders of magnitude after the first key tile (a reference left there
+    would overflow fp32), next to heads and a sequence of N(0, 1) rows in the
+    same launch."""
+    wl = W.towering_keys([1000, 500], seed=901)
+    rise = _first_tile_rise(wl)
+    assert all(rise[0, h].max() > 128.0 for h in range(6))
+    _check_against_rounded(attn, wl, "global")
+
+
+def test_aligned_keys_rise_past_the_first_tile(attn):
+    """Q and K along one direction per head: nearly every row's scores rise
+    more than 8 binary orders above its first tile's maximum, up to about
+    2^27, so the reference moves on nearly every row."""
+    wl = W.aligned_keys([1000, 300], seed=902)
+    rise = np.concatenate(list(_first_tile_rise(wl).values()))
+    assert (rise > 8.0).mean() > 0.9 and rise.max() > 20.0
+    _check_against_rounded(attn, wl, "global")
+
+
+def test_back_to_back_calls_do_not_share_state(attn):
+    """Calls with very different inputs queued back to back on one stream
+    give bit for bit what each gives on a fresh handle."""
+    aligned = W.aligned_keys([1000, 300], seed=902)
+    tower = W.towering_keys([1000, 500], seed=901)
+    ins = [(w.qkv.cuda(), w.cu_seqlens.cuda()) for w in (aligned, tower, aligned)]
+    outs = [attn.forward(q, cu, "global") for q, cu in ins]
+    torch.cuda.synchronize()
+    assert attn.get_error() == 0
+    fresh = binding.Attention(0)
+    try:
+        refs = [fresh.forward(q, cu, "global") for q, cu in ins[:2]]
+        torch.cuda.synchronize()
+        assert fresh.get_error() == 0
+    finally:
+        fresh.close()
+    assert torch.equal(outs[0], refs[0]) and torch.equal(outs[2], refs[0])
+    assert torch.equal(outs[1], refs[1])
