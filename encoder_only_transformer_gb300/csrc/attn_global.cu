@@ -22,8 +22,9 @@
 //               through 3-stage rings
 //   warps 9,10  MMA issuers, one per query tile (whole warp runs the loop;
 //               one elected lane issues): S_w = Q_w K^T, O_w += P_w V
-//   warp  11    idle (completes the third warpgroup, whose registers go to the
-//               softmax groups)
+//   warp  11    per segment, stages the score bound's inputs in shared
+//               memory: the norms of the segment's 256 rotated Q rows and the
+//               largest rotated K row norm of the head over the sequence
 // TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384)
 // O0 [384,448) O1 [448,512); fp32 except P (bf16 pairs).
 //
@@ -35,6 +36,15 @@
 // more than 8, so O and the row sum always share one reference.  Partial
 // states over disjoint key ranges are merged exactly:
 // m = max(m_a, m_b), O = O_a 2^(m_a - m) + O_b 2^(m_b - m), likewise l.
+// The reference may sit below a row's true maximum by any amount for which
+// 2^(score - reference) stays finite in the fp32 sums.  By Cauchy-Schwarz
+// every score of a row is at most |q| max|k| / 8 (norms of the rotated
+// rows, from the RoPE pass; the key maximum over the sequence).  After a
+// segment's second tile, a warp whose 32 rows all have that bound within
+// kSkipSlack (base 2) of their reference runs the segment's later tiles
+// without a row maximum and keeps its reference (weights up to 2^32).
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -50,7 +60,9 @@ constexpr uint32_t kOffQ = 0;                                  // 2 sets of (Q0,
 constexpr uint32_t kOffK = 4 * kTileBytes;                     // K ring
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;       // V ring
 constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;     // 163840
-constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
+constexpr uint32_t kNormSlotBytes = 4 * (2 * kBlockM + 4);    // 256 Q norms, max |k|, padding
+constexpr uint32_t kOffNorm = kOffBar + 512;                   // 2 slots of the score bound's inputs
+constexpr uint32_t kSmemBytes = kOffNorm + 2 * kNormSlotBytes + 1024;
 
 // barrier slots (8 bytes each) from kOffBar
 constexpr int kBarQFull = 0;      // + set (2)
@@ -67,7 +79,9 @@ constexpr int kBarOFree = 24;
 constexpr int kBarSegSync = 26;   // all 256 softmax threads wrote their partial rows
 constexpr int kBarSegFlag = 27;   // the counter result is in shared memory
 constexpr int kBarEarly = 28;     // the early look at the last segment's unit is in shared memory
-constexpr int kNumBars = 29;
+constexpr int kBarNormFull = 29;  // + slot (2): a segment's bound inputs staged
+constexpr int kBarNormEmpty = 31; // + slot: read by all 256 softmax threads
+constexpr int kNumBars = 33;
 constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;          // TMEM address
 constexpr uint32_t kOffFlag = kOffSlot + 8;                    // "I merge" flag
 constexpr uint32_t kOffEarly = kOffFlag + 4;                   // early-look result
@@ -81,6 +95,13 @@ constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false);
 constexpr uint32_t kIdescO = make_idesc_bf16(128, 64, true);
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
+// Largest exponent (base 2) a weight may take when the row maximum is
+// skipped: weights up to 2^32 keep the row sums of 2^31 keys (2^63) and the
+// P V sums of values below 2^60 finite in fp32.
+constexpr float kSkipSlack = 32.0f;
+// Relative margin on the bound for the fp32 rounding of the norms and of the
+// tensor-core sums (each far below 2^-16 relative).
+constexpr float kBoundMargin = 1.0f + 1.0f / 1024.0f;
 
 // ---------------------------------------------------------------- schedule
 struct Params {
@@ -91,6 +112,10 @@ struct Params {
     float *partials;
     __nv_bfloat16 *out;
     int32_t *err;
+    const float *norms;          // [12][norm_pitch]: rotated Q row norms per head
+    const uint16_t *knorm;       // [12][norm_pitch]: rotated K row norms, fp16 rounded up
+    long long norm_pitch;        // a multiple of 8
+    long long rows;              // rows of qkv (norms exist for rows below)
     int entries;
     long long total;             // iterations of all units
     int ctas;
@@ -290,6 +315,80 @@ __device__ void mma_issuer(const Ctx &c, const Params &p, int w, int cta)
     }
 }
 
+// ---------------------------------------------------------------- bound inputs
+// Non-blocking look at a barrier phase (acquire when it is complete).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// The bounded wait out of line: the hot loop only calls it when the staged
+// bound is late.
+__device__ __noinline__ bool slow_wait(uint32_t bar, uint32_t parity, int *err)
+{
+    return mbar_wait(bar, parity, err);
+}
+
+// Warp 11: for each segment, into shared-memory slot sg % 2, the norms of
+// the segment's 256 rotated Q rows (0 past the end of qkv, whose rows the
+// tensor map fills with zeros) and the largest rotated K row norm of its
+// head over the sequence (from fp16 norms rounded up; non-negative fp16
+// values order like their bits, +inf and NaN above all finite ones).
+__device__ void norm_stager(const Ctx &c, const Params &p, int lane, int cta)
+{
+    SegIter si;
+    si.init(p, cta);
+    Seg s;
+    for (uint32_t sg = 0; si.next(p, s); ++sg) {
+        const uint32_t slot = sg & 1;
+        if (sg >= 2 && !mbar_wait(bar(c, kBarNormEmpty + slot), ((sg >> 1) - 1) & 1, p.err))
+            return;
+        float *dst = reinterpret_cast<float *>(c.sbase + kOffNorm + slot * kNormSlotBytes);
+        const float *src = p.norms + s.head * p.norm_pitch;
+        const long long r0 = static_cast<long long>(s.row0) + s.q0;
+        float v[2 * kBlockM / 32];
+#pragma unroll
+        for (int j = 0; j < 2 * kBlockM / 32; ++j) {
+            const long long r = r0 + lane + 32 * j;
+            v[j] = r < p.rows ? src[r] : 0.f;
+        }
+        // K rows [lo, hi): the unaligned ends one by one, the rest 8 at a time
+        // (pairs of fp16 bit patterns, maxima taken two at a time)
+        const uint16_t *kn = p.knorm + s.head * p.norm_pitch;
+        const long long lo = s.row0, hi = static_cast<long long>(s.row0) + s.L;
+        const long long a0 = min((lo + 7) & ~7ll, hi), a1 = max(hi & ~7ll, a0);
+        uint32_t k0 = 0u, k1 = 0u;
+        if (lo + lane < a0)
+            k0 = kn[lo + lane];
+        if (a1 + lane < hi)
+            k1 = kn[a1 + lane];
+        const uint4 *kv = reinterpret_cast<const uint4 *>(kn + a0);
+        const int nv = static_cast<int>((a1 - a0) >> 3);
+#pragma unroll 8
+        for (int i = lane; i < nv; i += 32) {
+            const uint4 q8 = kv[i];
+            k0 = __vmaxu2(k0, __vmaxu2(q8.x, q8.y));
+            k1 = __vmaxu2(k1, __vmaxu2(q8.z, q8.w));
+        }
+        const uint32_t k2 = __vmaxu2(k0, k1);
+        const uint32_t kh = __reduce_max_sync(0xffffffffu, max(k2 & 0xFFFFu, k2 >> 16));
+        const float kmx = __half2float(__ushort_as_half(static_cast<unsigned short>(kh)));
+#pragma unroll
+        for (int j = 0; j < 2 * kBlockM / 32; ++j)
+            dst[lane + 32 * j] = v[j];
+        if (lane == 0)
+            dst[2 * kBlockM] = kmx;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar(c, kBarNormFull + slot));
+    }
+}
+
 // ---------------------------------------------------------------- softmax
 __device__ __forceinline__ float *partial_slot(const Params &p, int slot)
 {
@@ -333,10 +432,12 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
                          : "=r"(early_done) : "l"(p.unit_cnt + s.entry * kHeads + s.head) : "memory");
         float m = -INFINITY;    // running reference maximum (scaled, base 2)
         float l = 0.f;          // running sum of exp2(score - m)
-        for (int t = 0; t < n; ++t) {
+        // One key tile; with_max false leaves out the row maximum (the
+        // reference stays).  False when a wait gave up.
+        auto tile = [&](int t, auto with_max) -> bool {
             const uint32_t g = g0 + t;
             if (!mbar_wait(bar(c, kBarSFull + w), g & 1, p.err))
-                return;
+                return false;
             __syncwarp();
             tc_fence_after();
             float sc[kBlockN];
@@ -367,18 +468,21 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
             }
             // row maximum: 8 independent chains (columns 0-15 by 2-input
             // max, then 16 columns per step by 3-input max), then combine
-            float mp[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mp[k] = fmaxf(sc[k], sc[8 + k]);
-#pragma unroll
-            for (int i = 16; i < kBlockN; i += 16)
+            float mc = m;
+            if constexpr (decltype(with_max)::value) {
+                float mp[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mp[k] = fmax3(mp[k], sc[i + k], sc[i + 8 + k]);
-            const float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]),
-                                   fmaxf(fmax3(mp[3], mp[4], mp[5]), fmax3(mp[6], mp[7], mp[7])));
-            const float mc = mx * kScaleLog2;
+                    mp[k] = fmaxf(sc[k], sc[8 + k]);
+#pragma unroll
+                for (int i = 16; i < kBlockN; i += 16)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mp[k] = fmax3(mp[k], sc[i + k], sc[i + 8 + k]);
+                const float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]),
+                                       fmaxf(fmax3(mp[3], mp[4], mp[5]), fmax3(mp[6], mp[7], mp[7])));
+                mc = mx * kScaleLog2;
+            }
             const bool need = mc > m + kRescaleThreshold;
             const float mn = need ? mc : m;
             const float alpha = need ? ex2_approx(m - mn) : 1.f;
@@ -416,7 +520,7 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
             if (t > 0) {
                 // P_w and O_w are free once the previous P V has completed
                 if (!mbar_wait(bar(c, kBarODone + w), (g - 1) & 1, p.err))
-                    return;
+                    return false;
                 __syncwarp();
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, need)) {
@@ -438,6 +542,40 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(c, kBarPFull + w));
+            return true;
+        };
+        // Tiles with the row maximum up to the segment's second tile; then,
+        // when a later tile follows, the rows' score bound (staged by warp 11)
+        // decides whether the remaining tiles need a maximum.  The decision
+        // always falls at that tile, so the result does not depend on timing.
+        const uint32_t nslot = sg & 1, npar = (sg >> 1) & 1;
+        const float *nv = reinterpret_cast<const float *>(c.sbase + kOffNorm + nslot * kNormSlotBytes);
+        bool decided = false, skip = false;
+        int t = 0;
+        for (; t < n; ++t) {
+            if (!tile(t, std::true_type{}))
+                return;
+            if (!decided && t >= 1 && t + 1 < n) {
+                if (!__all_sync(0xffffffffu, mbar_test(bar(c, kBarNormFull + nslot), npar)) &&
+                    !slow_wait(bar(c, kBarNormFull + nslot), npar, p.err))
+                    return;
+                const float bound = nv[rr] * nv[2 * kBlockM] * (kScaleLog2 * kBoundMargin);
+                mbar_arrive(bar(c, kBarNormEmpty + nslot));
+                decided = true;
+                skip = __all_sync(0xffffffffu, bound <= m + kSkipSlack);
+                if (skip) {
+                    ++t;
+                    break;
+                }
+            }
+        }
+        for (; t < n; ++t)
+            if (!tile(t, std::false_type{}))
+                return;
+        if (!decided) {
+            if (!mbar_wait(bar(c, kBarNormFull + nslot), npar, p.err))
+                return;
+            mbar_arrive(bar(c, kBarNormEmpty + nslot));
         }
         g0 += n;
 
@@ -570,7 +708,8 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
                    const int32_t *__restrict__ cu, const int2 *__restrict__ work,
                    const int32_t *__restrict__ work_count, const int32_t *__restrict__ tile_start,
                    int32_t *__restrict__ unit_cnt, float *__restrict__ partials,
-                   __nv_bfloat16 *__restrict__ out, int32_t *err)
+                   __nv_bfloat16 *__restrict__ out, int32_t *err, const float *__restrict__ norms,
+                   const uint16_t *__restrict__ knorm, long long norm_pitch, long long rows)
 {
     pdl_wait();
     extern __shared__ uint8_t smem_raw[];
@@ -591,6 +730,10 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
     p.partials = partials;
     p.out = out;
     p.err = err;
+    p.norms = norms;
+    p.knorm = knorm;
+    p.norm_pitch = norm_pitch;
+    p.rows = rows;
     p.total = tile_start[p.entries];
     // split among at most `total` CTAs, so that every range is non-empty
     p.ctas = p.total < gridDim.x ? static_cast<int>(p.total) : static_cast<int>(gridDim.x);
@@ -623,6 +766,10 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
         mbar_init(bar(c, kBarSegSync), 2 * kBlockM);
         mbar_init(bar(c, kBarSegFlag), 1);
         mbar_init(bar(c, kBarEarly), 1);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(bar(c, kBarNormFull + q), 1);
+            mbar_init(bar(c, kBarNormEmpty + q), 2 * kBlockM);
+        }
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -642,6 +789,9 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
             __syncwarp();
         } else if (warp == 9 || warp == 10) {
             mma_issuer(c, p, warp - 9, cta);
+            __syncwarp();
+        } else {
+            norm_stager(c, p, lane, cta);
             __syncwarp();
         }
     } else {
@@ -669,7 +819,7 @@ cudaError_t launch_attn_global(const AttnArgs &a, cudaStream_t stream)
         return e;
     return launch_chained(attn_global_kernel, dim3(a.num_ctas), dim3(kThreads), kSmemBytes, stream,
         a.tm_rot, a.tm_qkv, a.cu, a.work, a.work_count, a.tile_start, a.unit_cnt, a.partials,
-        a.out, a.err);
+        a.out, a.err, a.norms, a.knorm, a.norm_pitch, a.rows);
 }
 
 }  // namespace mbert

@@ -49,6 +49,10 @@ struct mbert_attn {
     int32_t *unit_cnt = nullptr;            // [entries * heads]
     int64_t sk_cap = 0;                     // entries
     float *partials = nullptr;              // [2 * num_sms][kPartialFloats]
+    // global layers: norms of the rotated rows, for the score bound that
+    // lets the softmax skip its row maximum: Q fp32 [12][rot_cap], then K
+    // fp16 [12][rot_cap] (rot_cap a multiple of 8)
+    float *norms = nullptr;
     cudaStream_t last_stream = nullptr;
     EncodeTiledFn encode = nullptr;
     // measurement: event pairs around the attention kernel, per layer kind
@@ -145,17 +149,22 @@ int grow_workspace(mbert_attn *h, int64_t entries, int64_t rot_rows)
         }
     }
     if (rot_rows > h->rot_cap) {
-        int64_t cap = rot_rows < 8192 ? 8192 : rot_rows;
+        int64_t cap = rot_rows < 8192 ? 8192 : (rot_rows + 7) & ~static_cast<int64_t>(7);
         __nv_bfloat16 *r = nullptr;
-        if (cudaMalloc(&r, sizeof(__nv_bfloat16) * 2 * kHidden * cap) != cudaSuccess) {
+        float *nr = nullptr;
+        if (cudaMalloc(&r, sizeof(__nv_bfloat16) * 2 * kHidden * cap) != cudaSuccess ||
+            cudaMalloc(&nr, (sizeof(float) + sizeof(uint16_t)) * kHeads * cap) != cudaSuccess) {
             cudaGetLastError();
+            cudaFree(r);
             return MBERT_ERR_OOM;
         }
         if (h->rot) {
             cudaDeviceSynchronize();
             cudaFree(h->rot);
+            cudaFree(h->norms);
         }
         h->rot = r;
+        h->norms = nr;
         h->rot_cap = cap;
     }
     return MBERT_OK;
@@ -315,6 +324,7 @@ MBERT_API void mbert_attn_destroy(mbert_attn *h)
         cudaFree(h->work_count);
         cudaFree(h->work);
         cudaFree(h->rot);
+        cudaFree(h->norms);
         cudaFree(h->tile_start);
         cudaFree(h->unit_cnt);
         cudaFree(h->partials);
@@ -540,8 +550,18 @@ int forward_impl(mbert_attn *h, const void *qkv, const int32_t *cu_seqlens, int 
         h->last_stream = st;
         return e == cudaSuccess ? MBERT_OK : fail_cuda(e);
     }
+    float *norms = nullptr;
+    uint16_t *knorm = nullptr;
+    if (layer_kind == MBERT_GLOBAL) {
+        norms = h->norms;
+        knorm = reinterpret_cast<uint16_t *>(h->norms + kHeads * h->rot_cap);
+        a.norms = norms;
+        a.knorm = knorm;
+        a.norm_pitch = h->rot_cap;
+        a.rows = T;
+    }
     e = launch_plan_rope(p, static_cast<const __nv_bfloat16 *>(qkv), h->rope[layer_kind],
-                         h->cfg.max_seqlen, h->rot, st);
+                         h->cfg.max_seqlen, h->rot, norms, knorm, h->rot_cap, st);
     if (e == cudaSuccess && ev0)
         e = cudaEventRecord(ev0, st);
     if (e == cudaSuccess)

@@ -110,9 +110,13 @@ struct Plan {
 cudaError_t launch_plan(const Plan &p, cudaStream_t stream);
 
 // The plan and, in the same launch, the RoPE of Q and K of every row (all
-// heads) into rot[T][1536] bf16.
+// heads) into rot[T][1536] bf16.  With norms set (global layers), also the
+// Euclidean norm of every rotated row and head: Q head h in norms[h][row]
+// (fp32), K head h in knorm[h][row] (fp16 bits, rounded up), rows
+// `norm_pitch` apart (a multiple of 8).
 cudaError_t launch_plan_rope(const Plan &p, const __nv_bfloat16 *qkv, const float2 *table,
-                             int table_rows, __nv_bfloat16 *rot, cudaStream_t stream);
+                             int table_rows, __nv_bfloat16 *rot, float *norms, uint16_t *knorm,
+                             long long norm_pitch, cudaStream_t stream);
 
 // Admitted-key count per query row, from the attention kernels' tile
 // schedule and mask.
@@ -134,6 +138,10 @@ struct AttnArgs {
     const int32_t *tile_start = nullptr;
     int32_t *unit_cnt = nullptr;
     float *partials = nullptr;   // [2 * num_ctas][kPartialFloats]
+    const float *norms = nullptr;     // [12][norm_pitch]: rotated Q row norms per head
+    const uint16_t *knorm = nullptr;  // [12][norm_pitch]: rotated K row norms, fp16 rounded up
+    long long norm_pitch = 0;         // a multiple of 8
+    long long rows = 0;               // rows of qkv
 };
 
 // One partial state of a query block split across CTAs: O (unnormalised,

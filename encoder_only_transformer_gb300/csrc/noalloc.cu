@@ -199,7 +199,8 @@ MBERT_API int mbert_attn_forward_noalloc(const void *qkv, const int32_t *cu_seql
     // the work count and the error word must start at zero on every call
     cudaError_t e = cudaMemsetAsync(words, 0, 2 * sizeof(int32_t), st);
     if (e == cudaSuccess)
-        e = launch_plan_rope(p, static_cast<const __nv_bfloat16 *>(qkv), table, kTableRows, rot, st);
+        e = launch_plan_rope(p, static_cast<const __nv_bfloat16 *>(qkv), table, kTableRows, rot, nullptr,
+                             nullptr, 0, st);
     if (e == cudaSuccess)
         e = launch_attn_generic(a, st);
     if (e == cudaSuccess && device_status)

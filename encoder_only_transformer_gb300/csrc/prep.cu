@@ -174,44 +174,73 @@ constexpr int kRopeRowsPerCta = kPlanThreads / kRopeThreadsPerRow;   // 10 rows 
 // the result is rounded to bf16.  Positions come from cu_seqlens by binary
 // search; with cu_seqlens the plan rejects, the rows still land in rot[T]
 // (and the table index is clamped), and the attention kernel reads none.
+//
+// With `norms` set, the pass also records the Euclidean norm of every
+// rounded row and head: Q head h in norms[h][row] (fp32), K head h in
+// knorm[h][row] as fp16 rounded up (an upper bound: +inf past the fp16
+// range), rows `norm_pitch` apart.  By Cauchy-Schwarz |q . k| <= |q| |k|,
+// so these bound every score.
 __device__ void rope_block(long long b, const __nv_bfloat16 *__restrict__ qkv,
                            const int32_t *__restrict__ cu, int n_seqs, long long T,
-                           const float2 *__restrict__ table, int table_rows, __nv_bfloat16 *__restrict__ rot)
+                           const float2 *__restrict__ table, int table_rows, __nv_bfloat16 *__restrict__ rot,
+                           float *__restrict__ norms, uint16_t *__restrict__ knorm, long long norm_pitch)
 {
-    if (threadIdx.x >= kRopeRowsPerCta * kRopeThreadsPerRow)
-        return;
     const long long row = b * kRopeRowsPerCta + threadIdx.x / kRopeThreadsPerRow;
-    if (row >= T)
-        return;
-    const int sub = threadIdx.x % kRopeThreadsPerRow;
-    const int blk = sub >> 2;          // 0..11 Q heads, 12..23 K heads
-    const int chunk = sub & 3;         // pairs chunk*8 .. chunk*8+7
-    const int s = seq_of_row(cu, n_seqs, row);
-    int pos = static_cast<int>(row - __ldg(cu + s));
-    pos = min(max(pos, 0), table_rows - 1);
-    const int col = blk * kHeadDim + chunk * 8;
+    // whole warps drop out here: a row is three full warps
+    if (threadIdx.x < kRopeRowsPerCta * kRopeThreadsPerRow && row < T) {
+        const int sub = threadIdx.x % kRopeThreadsPerRow;
+        const int blk = sub >> 2;          // 0..11 Q heads, 12..23 K heads
+        const int chunk = sub & 3;         // pairs chunk*8 .. chunk*8+7
+        const int s = seq_of_row(cu, n_seqs, row);
+        int pos = static_cast<int>(row - __ldg(cu + s));
+        pos = min(max(pos, 0), table_rows - 1);
+        const int col = blk * kHeadDim + chunk * 8;
 
-    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(qkv + row * kQKVWidth + col));
-    const uint4 bb = __ldg(reinterpret_cast<const uint4 *>(qkv + row * kQKVWidth + col + kPairs));
-    const float4 *cs = reinterpret_cast<const float4 *>(table + static_cast<long long>(pos) * kPairs + chunk * 8);
-    const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t bv[4] = {bb.x, bb.y, bb.z, bb.w};
-    uint32_t ya[4], yb[4];
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(qkv + row * kQKVWidth + col));
+        const uint4 bb = __ldg(reinterpret_cast<const uint4 *>(qkv + row * kQKVWidth + col + kPairs));
+        const float4 *cs = reinterpret_cast<const float4 *>(table + static_cast<long long>(pos) * kPairs + chunk * 8);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t bv[4] = {bb.x, bb.y, bb.z, bb.w};
+        uint32_t ya[4], yb[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 t = __ldg(cs + i);          // (cos, sin) of pairs 2i, 2i+1
-        const float x0 = bf16lo_to_f32(av[i]), x1 = bf16hi_to_f32(av[i]);
-        const float z0 = bf16lo_to_f32(bv[i]), z1 = bf16hi_to_f32(bv[i]);
-        const float y0 = x0 * t.x - z0 * t.y;
-        const float y1 = x1 * t.z - z1 * t.w;
-        const float w0 = z0 * t.x + x0 * t.y;
-        const float w1 = z1 * t.z + x1 * t.w;
-        ya[i] = pack_bf16x2(y0, y1);
-        yb[i] = pack_bf16x2(w0, w1);
+        for (int i = 0; i < 4; ++i) {
+            const float4 t = __ldg(cs + i);          // (cos, sin) of pairs 2i, 2i+1
+            const float x0 = bf16lo_to_f32(av[i]), x1 = bf16hi_to_f32(av[i]);
+            const float z0 = bf16lo_to_f32(bv[i]), z1 = bf16hi_to_f32(bv[i]);
+            const float y0 = x0 * t.x - z0 * t.y;
+            const float y1 = x1 * t.z - z1 * t.w;
+            const float w0 = z0 * t.x + x0 * t.y;
+            const float w1 = z1 * t.z + x1 * t.w;
+            ya[i] = pack_bf16x2(y0, y1);
+            yb[i] = pack_bf16x2(w0, w1);
+        }
+        constexpr int kRotWidth = 2 * kHidden;
+        *reinterpret_cast<uint4 *>(rot + row * kRotWidth + col) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+        *reinterpret_cast<uint4 *>(rot + row * kRotWidth + col + kPairs) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+        if (norms) {
+            // squared norm of the 16 rounded values, then of the head's 64
+            // (the four chunk threads of a (row, head) are neighbouring lanes)
+            float sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float y0 = bf16lo_to_f32(ya[i]), y1 = bf16hi_to_f32(ya[i]);
+                const float w0 = bf16lo_to_f32(yb[i]), w1 = bf16hi_to_f32(yb[i]);
+                sq = fmaf(y0, y0, sq);
+                sq = fmaf(y1, y1, sq);
+                sq = fmaf(w0, w0, sq);
+                sq = fmaf(w1, w1, sq);
+            }
+            sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+            if (chunk == 0) {
+                const float nrm = sqrtf(sq);
+                if (blk < kHeads)
+                    norms[blk * norm_pitch + row] = nrm;
+                else
+                    knorm[(blk - kHeads) * norm_pitch + row] = __half_as_ushort(__float2half_ru(nrm));
+            }
+        }
     }
-    constexpr int kRotWidth = 2 * kHidden;
-    *reinterpret_cast<uint4 *>(rot + row * kRotWidth + col) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-    *reinterpret_cast<uint4 *>(rot + row * kRotWidth + col + kPairs) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
 }
 
 // The plan and the RoPE pass in one launch: block 0 builds the plan, blocks
@@ -221,13 +250,14 @@ plan_rope_kernel(const int32_t *__restrict__ cu, int n_seqs, long long T, int ma
                  int cu_short_ok, int32_t *err, int2 *__restrict__ work, int32_t *__restrict__ work_count,
                  int32_t *__restrict__ tile_start, int32_t *__restrict__ unit_cnt,
                  const __nv_bfloat16 *__restrict__ qkv, const float2 *__restrict__ table, int table_rows,
-                 __nv_bfloat16 *__restrict__ rot)
+                 __nv_bfloat16 *__restrict__ rot, float *__restrict__ norms, uint16_t *__restrict__ knorm,
+                 long long norm_pitch)
 {
     pdl_wait();
     if (blockIdx.x == 0)
         plan_block(cu, n_seqs, T, max_seqlen, blk, cu_short_ok, err, work, work_count, tile_start, unit_cnt);
     else
-        rope_block(blockIdx.x - 1, qkv, cu, n_seqs, T, table, table_rows, rot);
+        rope_block(blockIdx.x - 1, qkv, cu, n_seqs, T, table, table_rows, rot, norms, knorm, norm_pitch);
     pdl_trigger();
 }
 
@@ -312,12 +342,14 @@ cudaError_t launch_plan(const Plan &p, cudaStream_t stream)
 }
 
 cudaError_t launch_plan_rope(const Plan &p, const __nv_bfloat16 *qkv, const float2 *table,
-                             int table_rows, __nv_bfloat16 *rot, cudaStream_t stream)
+                             int table_rows, __nv_bfloat16 *rot, float *norms, uint16_t *knorm,
+                             long long norm_pitch, cudaStream_t stream)
 {
     const long long blocks = 1 + (p.T + kRopeRowsPerCta - 1) / kRopeRowsPerCta;
     return launch_chained(plan_rope_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kPlanThreads), 0, stream,
                           p.cu, p.n_seqs, p.T, p.max_seqlen, p.block, p.cu_short_ok ? 1 : 0, p.err, p.work,
-                          p.work_count, p.tile_start, p.unit_cnt, qkv, table, table_rows, rot);
+                          p.work_count, p.tile_start, p.unit_cnt, qkv, table, table_rows, rot, norms,
+                          knorm, norm_pitch);
 }
 
 cudaError_t launch_key_count(const Plan &p, int half_window, int32_t *counts, cudaStream_t stream)
