@@ -105,13 +105,13 @@ def towering_keys(lengths, seed: int, heads: int = 6, first: float = 0.05,
 
 
 def aligned_keys(lengths, seed: int, first: float = 0.2, later: float = 2.0,
-                 noise: float = 0.3) -> Workload:
+                 noise: float = 0.3, first_rows: int = 128) -> Workload:
     """Per head one random direction u (norm 8): every Q row is u plus
-    N(0, noise^2) noise, every K row `first` (the first 128 keys of each
-    sequence) or `later` times u plus noise; V ~ N(0, 1).  A key near the
-    query's own position then scores close to |q| |k| / 8, so the scores of
-    later key tiles rise far above those of the first tile while staying
-    close to the Cauchy-Schwarz bound of the norms."""
+    N(0, noise^2) noise, every K row `first` (the first `first_rows` keys of
+    each sequence) or `later` times u plus noise; V ~ N(0, 1).  A key near
+    the query's own position then scores close to |q| |k| / 8, so the
+    scores of later key tiles rise far above those of the first ones while
+    staying close to the Cauchy-Schwarz bound of the norms."""
     g = torch.Generator().manual_seed(seed)
     lengths = [int(L) for L in lengths]
     cu = cu_from_lengths(lengths)
@@ -125,7 +125,7 @@ def aligned_keys(lengths, seed: int, first: float = 0.2, later: float = 2.0,
         x[:, qc] = u + noise * torch.randn(T, 64, generator=g)
         scale = torch.full((T, 1), later)
         for b in cu[:-1].tolist():
-            scale[b:b + 128] = first
+            scale[b:b + first_rows] = first
         x[:, kc] = scale * (u + noise * torch.randn(T, 64, generator=g))
     return Workload(f"aligned{lengths}", seed, 1.0, lengths, ["global"], x.to(torch.bfloat16), cu)
 

@@ -364,6 +364,34 @@ def test_aligned_keys_rise_past_the_first_tile(attn):
     _check_against_rounded(attn, wl, "global")
 
 
+def test_skipped_maximum_with_large_weights(attn):
+    """The global kernel's skip of the row maximum with large weights: the
+    first 256 keys of each sequence are small, so after a segment's second
+    tile every row's Cauchy-Schwarz bound |q| max|k| / 8 lies within 32
+    (base 2) of its reference and the warps stop taking maxima, while the
+    later scores still rise more than 8 binary orders above that reference
+    (weights up to about 2^23, beyond anything the rescaling path forms)."""
+    wl = W.aligned_keys([1000, 300], seed=904, first=0.2, later=1.8, first_rows=256)
+    theta = oracle.KINDS["global"]["theta"]
+    cu = wl.cu_seqlens.tolist()
+    gap, rise = [], []
+    for s in range(len(cu) - 1):
+        b, e = cu[s], cu[s + 1]
+        x = wl.qkv[b:e].double().numpy()
+        for h in range(12):
+            q = oracle.round_bf16(_rotated(x[:, 64 * h:64 * h + 64], theta))
+            k = oracle.round_bf16(_rotated(x[:, 768 + 64 * h:768 + 64 * h + 64], theta))
+            sc = q @ k.T / 8.0 / LN2
+            ref = sc[:, :256].max(axis=1)
+            bound = np.linalg.norm(q, axis=1) * np.linalg.norm(k, axis=1).max() / 8.0 / LN2
+            gap.append(bound - ref)
+            rise.append(sc.max(axis=1) - ref)
+    gap, rise = np.concatenate(gap), np.concatenate(rise)
+    assert gap.max() < 31.0
+    assert (rise > 8.0).mean() > 0.9 and rise.max() > 20.0
+    _check_against_rounded(attn, wl, "global")
+
+
 def test_back_to_back_calls_do_not_share_state(attn):
     """Calls with very different inputs queued back to back on one stream
     give bit for bit what each gives on a fresh handle."""
