@@ -483,7 +483,8 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
                                        fmaxf(fmax3(mp[3], mp[4], mp[5]), fmax3(mp[6], mp[7], mp[7])));
                 mc = mx * kScaleLog2;
             }
-            const bool need = mc > m + kRescaleThreshold;
+            // (without the maximum the reference stays: no rescale at all)
+            const bool need = decltype(with_max)::value && mc > m + kRescaleThreshold;
             const float mn = need ? mc : m;
             const float alpha = need ? ex2_approx(m - mn) : 1.f;
             const float neg = -mn;
