@@ -287,6 +287,19 @@ __device__ void mma_issuer(const Ctx &c, const Params &p, int w, int cta)
                     return;
                 if (g > 0 && !mbar_wait(bar(c, kBarSEmpty + w), (g - 1) & 1, p.err))
                     return;
+                // Query tile 1's S of a key tile only once group 0 has
+                // loaded its own S of it: group 1 then trails group 0 by
+                // about one TMEM load, so that their exponential loops
+                // overlap less on the shared MUFU pipe than in lockstep.  Only
+                // where the tile and the two after it belong to this segment:
+                // group 0 may be up to two loads ahead (the K ring of 3 waits
+                // for group 1's S), and the parity wait then stands for the
+                // later phase, which group 0 reaches within the segment
+                // without anything from group 1.  Across a segment end it
+                // would wait on group 0's next segment, which waits on
+                // group 1.
+                if (w == 1 && t + 2 < n && !mbar_wait(bar(c, kBarSEmpty + 0), g & 1, p.err))
+                    return;
                 __syncwarp();
                 tc_fence_after();
                 issue_s(c, w, qs, st);
@@ -771,6 +784,7 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
             mbar_init(bar(c, kBarNormFull + q), 1);
             mbar_init(bar(c, kBarNormEmpty + q), 2 * kBlockM);
         }
+
         fence_mbar_init();
     }
     if (warp == 0) {
