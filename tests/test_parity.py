@@ -102,6 +102,21 @@ def test_many_tiny_sequences(attn, kind):
     _full_check(attn, W.custom(lengths, seed=78), kind)
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_global_split_schedules(attn, seed):
+    """Seeded packs of 2-60 sequences of 1-3000 tokens: the global kernel's
+    split of iterations among CTAs cuts units at every kind of place
+    (segments of one or two tiles, a CTA ending a unit's first tile, many
+    segment ends in a row), where its waits between the softmax groups
+    and the issuers must all complete: no device error, and sampled rows
+    against the oracle."""
+    g = torch.Generator().manual_seed(900 + seed)
+    n = int(torch.randint(2, 61, (1,), generator=g))
+    hi = [20, 300, 3000][seed % 3]
+    lengths = torch.randint(1, hi + 1, (n,), generator=g).tolist()
+    _sampled_check(attn, W.custom(lengths, seed=950 + seed), "global", per_seq=8, seed=seed)
+
+
 @pytest.mark.parametrize("kind", ["global", "local"])
 def test_length_one_returns_value_exactly(attn, kind):
     wl = W.custom([1, 1, 3, 1], seed=5)
