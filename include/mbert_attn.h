@@ -46,7 +46,8 @@ extern "C" {
 #endif
 
 /* Opaque handle: owns the two RoPE cos/sin tables, the device work-list
- * workspace, the rotated-operand scratch and the device error word. */
+ * workspace, the rotated-operand scratch (with the rotated rows' norms that
+ * global layers use to bound their scores) and the device error word. */
 typedef struct mbert_attn mbert_attn;
 
 /* Layer kinds.  Layer i of the 22-layer stack is global iff i % 3 == 0
