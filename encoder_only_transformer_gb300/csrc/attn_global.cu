@@ -3,9 +3,11 @@
 //
 // Work: a unit is (work entry, head), an entry being 256 query rows of one
 // sequence; a unit needs ceil(L/128) key tiles.  All (unit, key tile)
-// iterations, in work-list order, are split into equal contiguous ranges, one
-// per persistent CTA (one CTA per SM), so every SM gets the same number of
-// tile iterations whatever the number of units.  A CTA walks its range as a
+// iterations, in work-list order, are split into contiguous ranges, one per
+// persistent CTA (one CTA per SM), of equal cost whatever the number of
+// units: a range's cost is its iterations plus kSegCost for each unit that
+// starts inside it (each extra segment costs a Q load, an epilogue and a
+// pipeline refill).  A CTA walks its range as a
 // sequence of segments (a unit and a run of its key tiles).  A segment that
 // covers its whole unit writes the output directly; a unit cut between CTAs
 // leaves one partial state (unnormalised O, row maximum, row sum) per
@@ -102,6 +104,9 @@ constexpr float kSkipSlack = 32.0f;
 // Relative margin on the bound for the fp32 rounding of the norms and of the
 // tensor-core sums (each far below 2^-16 relative).
 constexpr float kBoundMargin = 1.0f + 1.0f / 1024.0f;
+// Cost of a segment's fixed work (Q load, epilogue, pipeline refill) in key
+// tile iterations, for the split of the iterations among CTAs.
+constexpr int kSegCost = 4;
 
 // ---------------------------------------------------------------- schedule
 struct Params {
@@ -119,22 +124,56 @@ struct Params {
     int entries;
     long long total;             // iterations of all units
     int ctas;
+    int alpha;                   // cost of a unit start inside a range (kSegCost or 0)
+    long long cost;              // total + alpha * (units - 1)
 };
 
-__device__ __forceinline__ long long range_lo(const Params &p, int c)
+// The split is made in cost coordinates: iteration `it` of unit u sits at
+// x = it + alpha * u, so each unit start adds alpha.  CTA c owns the
+// iterations whose x lies in [x_lo(c), x_lo(c + 1)).
+__device__ __forceinline__ long long x_lo(const Params &p, int c)
 {
-    return static_cast<long long>(c) * p.total / p.ctas;
+    return static_cast<long long>(c) * p.cost / p.ctas;
 }
 
-// The CTA whose range contains iteration `it`.
-__device__ __forceinline__ int cta_of(const Params &p, long long it)
+// The CTA whose range contains iteration `it` of unit `u`: the largest c
+// with floor(c * cost / ctas) <= x.
+__device__ __forceinline__ int cta_of(const Params &p, long long it, int u)
 {
-    int c = static_cast<int>((it * p.ctas) / p.total);
-    while (c + 1 < p.ctas && range_lo(p, c + 1) <= it)
-        ++c;
-    while (c > 0 && range_lo(p, c) > it)
-        --c;
-    return c;
+    const long long x = it + static_cast<long long>(p.alpha) * u;
+    const long long c = ((x + 1) * p.ctas - 1) / p.cost;
+    return c < p.ctas - 1 ? static_cast<int>(c) : p.ctas - 1;
+}
+
+// The first iteration at or after cost coordinate x, and the entry holding it
+// (p.entries for x = cost, the end).  Entry e starts at x = tile_start[e] +
+// alpha * heads * e; x values between two units map to the later unit's start.
+__device__ long long iter_at(const Params &p, long long x, int &entry)
+{
+    const long long per = static_cast<long long>(p.alpha) * kHeads;
+    // a guess as if all entries cost the same (exact for one sequence; two
+    // independent loads), then a binary search on the side it missed
+    int e = min(static_cast<int>((x * p.entries) / p.cost), p.entries - 1);
+    long long t0 = p.tile_start[e], t1 = p.tile_start[e + 1];
+    if (!(t0 + per * e <= x && x < t1 + per * (e + 1))) {
+        int lo = 0, h = p.entries;
+        while (h - lo > 1) {
+            const int mid = (lo + h) >> 1;
+            if (p.tile_start[mid] + per * mid <= x)
+                lo = mid;
+            else
+                h = mid;
+        }
+        e = lo;
+        t0 = p.tile_start[e];
+        t1 = p.tile_start[e + 1];
+    }
+    const long long n = (t1 - t0) / kHeads;           // iterations of each unit of the entry
+    const long long d = x - t0 - per * e;
+    const long long h = min(static_cast<long long>(kHeads - 1), d / (n + p.alpha));
+    const long long r = d - h * (n + p.alpha);
+    entry = (r >= n && h == kHeads - 1) ? e + 1 : e;
+    return t0 + h * n + (r < n ? r : n);
 }
 
 // A run of key tiles [kb, ke) of one unit.
@@ -151,26 +190,9 @@ struct SegIter {
 
     __device__ void init(const Params &p, int c)
     {
-        it = range_lo(p, c);
-        hi = range_lo(p, c + 1);
-        // the entry with tile_start <= it < its successor's: first a guess
-        // as if all entries had the same iterations (exact for one sequence,
-        // two independent loads), then a binary search on the side it missed
-        const int e = min(static_cast<int>((it * p.entries) / p.total), p.entries - 1);
-        const long long t0 = p.tile_start[e], t1 = p.tile_start[e + 1];
-        if (t0 <= it && it < t1) {
-            entry = e;
-            return;
-        }
-        int lo = it < t0 ? 0 : e + 1, h = it < t0 ? e : p.entries;
-        while (h - lo > 1) {
-            const int mid = (lo + h) >> 1;
-            if (p.tile_start[mid] <= it)
-                lo = mid;
-            else
-                h = mid;
-        }
-        entry = lo;
+        int e_hi;
+        it = iter_at(p, x_lo(p, c), entry);
+        hi = iter_at(p, x_lo(p, c + 1), e_hi);
     }
 
     __device__ bool next(const Params &p, Seg &s)
@@ -408,11 +430,13 @@ __device__ __forceinline__ float *partial_slot(const Params &p, int slot)
     return p.partials + static_cast<size_t>(slot) * kPartialFloats;
 }
 
-// Slot used by CTA cc for the unit starting at iteration ua: its first slot
-// when the unit is (or starts) its first segment, else its second.
-__device__ __forceinline__ int slot_of(const Params &p, int cc, long long ua)
+// Slot used by CTA cc for unit u, starting at iteration ua: its first slot
+// when the unit is (or starts) its first segment, else its second.  CTA cc's
+// range starts at or after ua when x_lo(cc) lies past the last iteration
+// before the unit (ua - 1, of unit u - 1).
+__device__ __forceinline__ int slot_of(const Params &p, int cc, long long ua, int u)
 {
-    return range_lo(p, cc) >= ua ? 2 * cc : 2 * cc + 1;
+    return (ua == 0 || x_lo(p, cc) >= ua + static_cast<long long>(p.alpha) * (u - 1)) ? 2 * cc : 2 * cc + 1;
 }
 
 __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_group,
@@ -618,7 +642,7 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
         if (early) {
             if (looker) {
                 *reinterpret_cast<volatile int *>(c.sbase + kOffEarly) =
-                    early_done == cta_of(p, s.ua + s.ntiles - 1) - cta;
+                    early_done == cta_of(p, s.ua + s.ntiles - 1, s.entry * kHeads + s.head) - cta;
                 mbar_arrive(bar(c, kBarEarly));
             }
             if (!mbar_wait(bar(c, kBarEarly), 0, p.err))
@@ -630,8 +654,9 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
             // the workspace, and merge if this is the unit's last segment
             // (known from the early look, or from the unit's counter).
             const long long ua = s.ua, ub = s.ua + s.ntiles;
+            const int unit = s.entry * kHeads + s.head;
             if (!merge_now) {
-                float *mine = partial_slot(p, slot_of(p, cta, ua));
+                float *mine = partial_slot(p, slot_of(p, cta, ua, unit));
                 float4 *dst = reinterpret_cast<float4 *>(mine + rr * kHeadDim);
 #pragma unroll
                 for (int i = 0; i < kHeadDim / 4; ++i)
@@ -645,9 +670,8 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
                 if (!merge_now) {
                     last = 0;
                     if (mbar_wait(bar(c, kBarSegSync), npartial & 1, p.err)) {
-                        const int c_first = cta_of(p, ua), c_last = cta_of(p, ub - 1);
+                        const int c_first = cta_of(p, ua, unit), c_last = cta_of(p, ub - 1, unit);
                         const int nseg = c_last - c_first + 1;
-                        const int unit = s.entry * kHeads + s.head;
                         last = atomicAdd(p.unit_cnt + unit, 1) == nseg - 1;
                         __threadfence();
                     }
@@ -666,7 +690,7 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
                 // usual case: its last segment is the unit's first), its own
                 // state is already the running state; the first merge step
                 // would reproduce it exactly (weights 0 and 1).
-                const int c_first = cta_of(p, ua), c_last = cta_of(p, ub - 1);
+                const int c_first = cta_of(p, ua, unit), c_last = cta_of(p, ub - 1, unit);
                 int cc = c_first;
                 if (c_first == cta) {
                     ++cc;
@@ -678,7 +702,7 @@ __device__ void softmax_group(const Ctx &c, const Params &p, int w, int warp_in_
                         o[i] = 0.f;
                 }
                 for (; cc <= c_last; ++cc) {
-                    const float *part = partial_slot(p, slot_of(p, cc, ua));
+                    const float *part = partial_slot(p, slot_of(p, cc, ua, unit));
                     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(part + kPartialRows * kHeadDim) + rr);
                     const float mnew = fmaxf(m, ml.x);
                     const float a = cc == c_first ? 0.f : ex2_approx(m - mnew);
@@ -751,6 +775,15 @@ attn_global_kernel(const __grid_constant__ CUtensorMap tm_rot,
     p.total = tile_start[p.entries];
     // split among at most `total` CTAs, so that every range is non-empty
     p.ctas = p.total < gridDim.x ? static_cast<int>(p.total) : static_cast<int>(gridDim.x);
+    // weigh unit starts only where every range stays non-empty: with
+    // cost >= (alpha + 1) * ctas consecutive range starts lie more than one
+    // inter-unit gap apart in cost coordinates
+    {
+        const long long extra = static_cast<long long>(kSegCost) * (static_cast<long long>(kHeads) * p.entries - 1);
+        const bool weigh = p.total + extra >= static_cast<long long>(kSegCost + 1) * p.ctas;
+        p.alpha = weigh ? kSegCost : 0;
+        p.cost = p.total + (weigh ? extra : 0);
+    }
     const int cta = blockIdx.x;
     if (cta >= p.ctas)
         return;
