@@ -117,6 +117,18 @@ def test_global_split_schedules(attn, seed):
     _sampled_check(attn, W.custom(lengths, seed=950 + seed), "global", per_seq=8, seed=seed)
 
 
+@pytest.mark.parametrize("lengths", [[1024], [1025], [1280], [1025, 3, 257, 640]])
+def test_global_split_weighting_edge(attn, lengths):
+    """The global kernel splits its iterations into ranges of equal cost,
+    counting each unit start inside a range as extra iterations, but only
+    where every range stays non-empty.  On 152 CTAs a single sequence of 1024
+    tokens (4 query blocks) falls back to ranges of equal iterations and one
+    of 1025 (5 blocks) is the first to be weighted; 1280 and the mixed pack
+    put range starts between units, including at entry boundaries.  Sampled
+    rows against the oracle on both sides."""
+    _sampled_check(attn, W.custom(lengths, seed=960 + sum(lengths)), "global", per_seq=96, seed=7)
+
+
 @pytest.mark.parametrize("kind", ["global", "local"])
 def test_length_one_returns_value_exactly(attn, kind):
     wl = W.custom([1, 1, 3, 1], seed=5)
