@@ -488,7 +488,8 @@ int forward_impl(mbert_attn *h, const void *qkv, const int32_t *cu_seqlens, int 
     p.cu_short_ok = cu_short;
     if (layer_kind == MBERT_GLOBAL) {
         // the global kernel takes 256 query rows (two 128-row tiles) per
-        // entry and splits all iterations evenly among one CTA per SM
+        // entry and splits all iterations among one CTA per SM into
+        // ranges of equal cost
         p.block = 2 * kBlockM;
         p.entry_bound = static_cast<int>((T + (p.block - 1) * static_cast<int64_t>(n_seqs)) / p.block);
         p.tile_start = h->tile_start;
